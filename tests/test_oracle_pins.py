@@ -1,0 +1,353 @@
+"""Pins of the CPU oracle to things other than itself (no GPU).
+
+Each test checks one oracle function against what the pages fix, a closed form, a
+library routine on a special case, exact rational arithmetic, or brute force, chosen
+so that a dropped term, a wrong sign or index, or a transposed operand fails.
+"""
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from synth import inputs as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------- number formats
+
+
+def test_e2m1_codebook_matches_ocp_fixture():
+    vals = _golden("e2m1_codebook.json")["values"]
+    assert O.E2M1.tolist() == vals
+    # sign bit: v(c + 8) = -v(c); largest magnitude 6
+    for c in range(8):
+        assert O.E2M1[c + 8] == -O.E2M1[c]
+        assert math.copysign(1.0, O.E2M1[c + 8]) == -1.0
+    assert np.abs(O.E2M1).max() == 6.0
+
+
+def test_e4m3_matches_torch_decode_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and nan[0x7F] and nan[0xFF]
+    assert np.isnan(O.E4M3[nan]).all()
+    np.testing.assert_array_equal(O.E4M3[~nan], ref[~nan])
+    assert O.E4M3[0x38] == 1.0 and O.E4M3[0x7E] == 448.0 and O.E4M3[0x01] == 2.0 ** -9
+
+
+def test_e4m3_roundtrip_of_generator_scales():
+    _, scales = S.expert_weights(7, 1, 0, 64, 256)
+    v = O.E4M3[scales]
+    assert v.min() >= 0.25 and v.max() <= 2.0
+    # the generator's encode of the decoded values is the identity
+    np.testing.assert_array_equal(S.e4m3_bits_from_f32(v), scales)
+
+
+def test_round_to_bf16_matches_torch():
+    g = np.random.default_rng(0)
+    x = np.concatenate([
+        (g.standard_normal(20000) * np.exp2(g.integers(-30, 30, 20000))).astype(np.float32),
+        # exact ties between two BF16 neighbours, both parities
+        ((np.arange(1, 4000, dtype=np.uint32) << 16) | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38, 1e-40, -1e-45], dtype=np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), ref)
+
+
+def test_bf16_bits_decode():
+    bits = S.bf16_bits_from_f32(np.array([1.0, -2.5, 0.15625, 3e38], dtype=np.float32))
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_bits_to_f64(bits), ref)
+
+
+# ---------------------------------------------------------------------------- dequantisation
+
+
+@pytest.mark.parametrize("case", _golden("layout_pins.json")["cases"], ids=lambda c: c["name"])
+def test_dequant_layout_pins(case):
+    packed = np.array(case["packed"], dtype=np.uint8)
+    scales = np.array(case["scales"], dtype=np.uint8)
+    w = O.dequant_nvfp4(packed, scales, case["scale2"], "exact")
+    assert w.shape == (case["N"], case["K"])
+    for (n, k), v in zip(case["expect_index"], case["expect_value"]):
+        assert w[n, k] == v, (n, k, w[n, k], v)
+
+
+def _dequant_rational(packed, scales, s2, n, k):
+    """One weight as an exact rational, then rounded the way the pages state."""
+    K = packed.shape[1] * 2
+    byte = int(packed[n, k // 2])
+    nib = (byte & 0xF) if k % 2 == 0 else (byte >> 4)
+    return Fraction(float(O.E2M1[nib])) * Fraction(float(O.E4M3[scales[n, k // 16]])) * Fraction(float(s2))
+
+
+def test_dequant_multiply_order_and_rounding():
+    """fp32(fp32(lut * e4m3) * scale2): lut*e4m3 is exact, so the value is the exact
+    triple product rounded once to fp32 (and then to BF16 for the bf16 variant)."""
+    g = np.random.default_rng(1)
+    N, K = 8, 64
+    packed = g.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = g.integers(0x20, 0x50, (N, K // 16), dtype=np.uint8)
+    s2 = np.float32(0.0030518)  # not a power of two
+    we = O.dequant_nvfp4(packed, scales, s2, "exact")
+    wb = O.dequant_nvfp4(packed, scales, s2, "bf16")
+    for n in range(N):
+        for k in range(K):
+            exact = _dequant_rational(packed, scales, s2, n, k)
+            f32 = np.float32(float(exact))  # round-to-nearest of the exact product
+            # float(Fraction) rounds to nearest double; the double of a 30-bit product is
+            # exact, so the float32 cast is the single correct rounding
+            assert we[n, k] == f32
+            assert wb[n, k] == O.round_to_bf16(np.array([f32]))[0]
+
+
+# ---------------------------------------------------------------------------- routing
+
+
+def test_router_logits_exact_integers():
+    g = np.random.default_rng(2)
+    x = g.integers(-3, 4, (5, 64)).astype(np.float32)
+    w = g.integers(-2, 3, (7, 64)).astype(np.float32)
+    lg = O.router_logits(S.bf16_bits_from_f32(x), S.bf16_bits_from_f32(w))
+    ref = [[sum(int(x[t, h]) * int(w[e, h]) for h in range(64)) for e in range(7)] for t in range(5)]
+    np.testing.assert_array_equal(lg, np.array(ref, dtype=np.float32))
+
+
+def _topk_brute(key_row, k):
+    order = sorted(range(len(key_row)), key=lambda e: (-float(key_row[e]), e))
+    return order[:k]
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_route_topk_brute_force(with_bias):
+    g = np.random.default_rng(3)
+    T, E, k = 40, 12, 4
+    logits = g.integers(-4, 5, (T, E)).astype(np.float32)  # many ties
+    bias = g.integers(-1, 2, E).astype(np.float32) if with_bias else None
+    ids, wts = O.route_topk(logits, k, bias)
+    for t in range(T):
+        key = logits[t] + (bias if bias is not None else 0)
+        assert ids[t].tolist() == _topk_brute(key, k)
+        sel = [math.exp(float(logits[t, e])) for e in ids[t]]
+        ref = [v / sum(sel) for v in sel]  # renormalised over the selected, unbiased
+        np.testing.assert_allclose(wts[t], ref, rtol=1e-12)
+    np.testing.assert_allclose(wts.sum(1), 1.0, rtol=1e-12)
+
+
+def test_route_topk_full_softmax_and_scale():
+    g = np.random.default_rng(4)
+    logits = g.standard_normal((6, 9)).astype(np.float32)
+    ids, wts = O.route_topk(logits, 9, routed_scale=2.5)
+    for t in range(6):
+        assert sorted(ids[t].tolist()) == list(range(9))
+        full = np.exp(logits[t].astype(np.float64)) / np.exp(logits[t].astype(np.float64)).sum()
+        np.testing.assert_allclose(wts[t], 2.5 * full[ids[t]], rtol=1e-12)
+    # without renormalisation the k weights are the full-E softmax values
+    ids3, w3 = O.route_topk(logits, 3, renormalize=0)
+    for t in range(6):
+        full = np.exp(logits[t].astype(np.float64)) / np.exp(logits[t].astype(np.float64)).sum()
+        np.testing.assert_allclose(w3[t], full[ids3[t]], rtol=1e-12)
+        assert w3[t].sum() < 1.0
+
+
+def test_route_topk_rejects_nan():
+    lg = np.zeros((2, 4), np.float32)
+    lg[1, 2] = np.nan
+    with pytest.raises(ValueError):
+        O.route_topk(lg, 2)
+
+
+# ---------------------------------------------------------------------------- sort
+
+
+def _sort_brute(ids, E):
+    """Plain counting sort: count, exclusive prefix, then place slots in flat order."""
+    T, k = ids.shape
+    cnt = [0] * (E + 1)
+    for i in range(T * k):
+        e = int(ids.flat[i])
+        cnt[e if e >= 0 else E] += 1
+    off = [0]
+    for e in range(E + 1):
+        off.append(off[-1] + cnt[e])
+    fill = [0] * (E + 1)
+    st, se, tp = [0] * (T * k), [0] * (T * k), [0] * (T * k)
+    for i in range(T * k):
+        e = int(ids.flat[i])
+        b = e if e >= 0 else E
+        p = off[b] + fill[b]
+        fill[b] += 1
+        st[p], se[p] = i // k, e
+        tp[i] = p if e >= 0 else -1
+    return st, se, off[:E + 1], tp
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_sort_brute_force_and_invariants(seed):
+    g = np.random.default_rng(seed)
+    T, k, E = 37, 3, 7
+    ids = g.integers(-1 if seed == 2 else 0, E, (T, k)).astype(np.int32)
+    r = O.sort_by_expert(ids, E)
+    st, se, off, tp = _sort_brute(ids, E)
+    assert r["sorted_token_ids"].tolist() == st
+    assert r["sorted_expert_ids"].tolist() == se
+    assert r["expert_offsets"].tolist() == off
+    assert r["token_to_perm"].reshape(-1).tolist() == tp
+    # invariants
+    o = r["expert_offsets"]
+    assert o[0] == 0 and (np.diff(o) >= 0).all() and o[E] == (ids >= 0).sum()
+    valid = ids.reshape(-1) >= 0
+    p = r["token_to_perm"].reshape(-1)[valid]
+    assert sorted(p.tolist()) == list(range(int(o[E])))
+    flat = np.arange(T * k)[valid]
+    np.testing.assert_array_equal(r["sorted_token_ids"][p], flat // k)
+    np.testing.assert_array_equal(r["sorted_expert_ids"][p], ids.reshape(-1)[valid])
+    for e in range(E):
+        assert (r["sorted_expert_ids"][o[e]:o[e + 1]] == e).all()
+
+
+def test_sort_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        O.sort_by_expert(np.array([[0, 5]], np.int32), 5)
+
+
+# ---------------------------------------------------------------------------- grouped GEMM
+
+
+def test_grouped_gemm_exact_dyadic_case():
+    """All scales 1.0 (0x38), scale2 = 1, x in {-2..2}: every product and partial sum is a
+    small dyadic rational, so the result equals exact integer/rational arithmetic."""
+    g = np.random.default_rng(5)
+    T, E, k, N, K = 9, 4, 2, 8, 64
+    ids = S.distinct_ids(g, T, E, k)
+    x = g.integers(-2, 3, (T, K)).astype(np.float32)
+    packed = [g.integers(0, 256, (N, K // 2), dtype=np.uint8) for _ in range(E)]
+    scales = [np.full((N, K // 16), 0x38, np.uint8) for _ in range(E)]
+    r = O.sort_by_expert(ids, E)
+    wfn = lambda e: O.dequant_nvfp4(packed[e], scales[e], 1.0, "bf16")
+    out = O.grouped_gemm(x.astype(np.float64), r["expert_offsets"], wfn, r["sorted_token_ids"])
+    for p in range(T * k):
+        t, e = int(r["sorted_token_ids"][p]), int(r["sorted_expert_ids"][p])
+        for n in range(N):
+            acc = Fraction(0)
+            for kk in range(K):
+                byte = int(packed[e][n, kk // 2])
+                nib = (byte & 0xF) if kk % 2 == 0 else (byte >> 4)
+                acc += Fraction(int(x[t, kk])) * Fraction(float(O.E2M1[nib]))
+            assert out[p, n] == float(acc)
+
+
+def test_grouped_gemm_brute_force_dense():
+    """Dense dequant-then-matmul per (token, slot) with no sort must match the sorted
+    grouped output read back through token_to_perm."""
+    c = S.make_gemm_case(T=5, E=4, k=2, N=16, K=64, seed=11)
+    r = O.sort_by_expert(c.ids, c.E)
+    x = O.bf16_bits_to_f64(c.x)
+    dense = [O.dequant_nvfp4(c.w.packed[e], c.w.scales[e], c.w.scale2[e], "bf16") for e in range(c.E)]
+    out = O.grouped_gemm(x, r["expert_offsets"], lambda e: dense[e], r["sorted_token_ids"])
+    for t in range(c.T):
+        for s in range(c.k):
+            e = int(c.ids[t, s])
+            ref = [sum(x[t, kk] * float(dense[e][n, kk]) for kk in range(c.K)) for n in range(c.N)]
+            np.testing.assert_allclose(out[r["token_to_perm"][t, s]], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_grouped_gemm_absent_expert_rows_zero():
+    c = S.make_gemm_case(T=6, E=4, k=2, N=8, K=32, seed=12, absent=(1,))
+    r = O.sort_by_expert(c.ids, c.E)
+    wfn = lambda e: None if c.w.packed[e] is None else O.dequant_nvfp4(c.w.packed[e], c.w.scales[e], c.w.scale2[e])
+    out = O.grouped_gemm(O.bf16_bits_to_f64(c.x), r["expert_offsets"], wfn, r["sorted_token_ids"])
+    o = r["expert_offsets"]
+    assert (out[o[1]:o[2]] == 0).all() and o[2] > o[1]
+    assert (np.abs(out[o[0]:o[1]]).sum(1) > 0).all()
+
+
+# ---------------------------------------------------------------------------- SwiGLU, combine
+
+
+def test_swiglu_special_values():
+    L = 7.0
+    silu = lambda z: z / (1.0 + math.exp(-z))
+    g = np.array([10.0, 7.0, 0.0, -3.0, -50.0, 2.0, 2.0])
+    u = np.array([1.0, 2.0, 5.0, 1.0, 1.0, 9.0, -9.0])
+    out = O.swiglu_clamp(g, u, L)
+    assert out[0] == silu(7.0) * 1.0  # gate clamped at +L
+    assert out[1] == silu(7.0) * 2.0
+    assert out[2] == 0.0
+    assert out[3] == pytest.approx(silu(-3.0))  # no lower clamp on the gate
+    assert out[4] == pytest.approx(silu(-50.0))
+    assert out[5] == silu(2.0) * 7.0 and out[6] == silu(2.0) * -7.0  # up clamps at +-L
+
+
+def test_combine_k1_unpermutes_and_weights():
+    g = np.random.default_rng(6)
+    T, H = 7, 5
+    y = g.standard_normal((T, H))
+    perm = g.permutation(T).astype(np.int32).reshape(T, 1)
+    out = O.combine_indexed(y, perm, np.ones((T, 1)))
+    np.testing.assert_array_equal(out, y[perm[:, 0]])
+    # k = 3 brute force with a -1 slot
+    perm3 = np.stack([g.permutation(T) for _ in range(3)], 1).astype(np.int32)
+    perm3[2, 1] = -1
+    w3 = g.random((T, 3))
+    out3 = O.combine_indexed(y, perm3, w3)
+    for t in range(T):
+        ref = sum(w3[t, s] * y[perm3[t, s]] for s in range(3) if perm3[t, s] >= 0)
+        np.testing.assert_allclose(out3[t], ref, rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------- whole path
+
+
+def test_forward_single_expert_is_dense_swiglu_mlp():
+    """E = 1, k = 1: routing picks expert 0 with weight 1 and the sort is the identity, so
+    the path is a textbook dense SwiGLU MLP (computed here with torch, fp64)."""
+    c = S.make_block_case(T=6, H=64, I=32, E=1, k=1, routing="biased", seed=13)
+    res = O.prefill_forward(c, "exact")
+    assert res["ids"].tolist() == [[0]] * 6 and np.allclose(res["wts"], 1.0)
+    x = torch.from_numpy(O.bf16_bits_to_f64(c.x))
+    wgu = torch.from_numpy(O.dequant_nvfp4(c.gate_up.packed[0], c.gate_up.scales[0], c.gate_up.scale2[0], "exact")).double()
+    wd = torch.from_numpy(O.dequant_nvfp4(c.down.packed[0], c.down.scales[0], c.down.scale2[0], "exact")).double()
+    f32 = lambda t: t.float().double()  # stage boundary of the exact variant
+    h = f32(x @ wgu.T)
+    gate, up = torch.clamp(h[:, :32], max=7.0), torch.clamp(h[:, 32:], -7.0, 7.0)
+    act = f32(torch.nn.functional.silu(gate) * up)
+    y = f32(act @ wd.T)
+    np.testing.assert_allclose(res["out64"], y.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_token_forward_matches_sorted_forward():
+    c = S.make_block_case(T=12, H=64, I=32, E=6, k=3, routing="biased", seed=14)
+    res = O.prefill_forward(c, "bf16")
+    tok = O.token_forward(c, [0, 5, 11], res["ids"], res["wts"], "bf16")
+    np.testing.assert_allclose(tok["out64"], res["out64"][[0, 5, 11]], rtol=1e-12, atol=1e-12)
+
+
+def test_bf16_variant_gap_matches_pages_scale():
+    """At the pages' measured shape, the BF16-weight and exact oracles differ by about the
+    weight-rounding share of the pages' table (grouped vs exact 0.0033 vs 0.0023 BF16-weight):
+    a few 1e-3 of the largest output, not 1e-5 and not 1e-2."""
+    c = S.workload("c0")
+    r = O.sort_by_expert(c.ids, c.E)
+    x = O.bf16_bits_to_f64(c.x)
+    outs = {}
+    for v in O.VARIANTS:
+        wfn = lambda e, v=v: O.dequant_nvfp4(c.w.packed[e], c.w.scales[e], c.w.scale2[e], v)
+        outs[v] = O.grouped_gemm(x, r["expert_offsets"], wfn, r["sorted_token_ids"])
+    gap = np.abs(outs["bf16"] - outs["exact"]).max() / np.abs(outs["exact"]).max()
+    tab = _golden("grouped_gemm_error_table.json")["rows"]
+    assert 3e-4 < gap < tab["grouped_vs_exact_fp32"][1]

@@ -1,0 +1,266 @@
+/*
+ * moe_prefill.h -- C ABI of the GB300 (sm_103a) routed-MoE NVFP4 (W4A16) prefill library.
+ *
+ * One chunk of prefill rows runs: top-k routing -> stable expert sort -> one grouped W4A16
+ * gate/up GEMM over all experts (activations gathered in the kernel through
+ * sorted_token_ids) -> clamped SwiGLU -> one grouped down GEMM -> routing-weighted combine
+ * back to token order.  The operations follow the web pages "Module forward_prefill_gemm"
+ * (module docs and source of spark_model::layers::glm5next_mlp::forward_prefill_gemm) and
+ * the two "glm5next_mlp/forward.rs" pages (spark_model, older; metrale_model_arch, newer).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked "device" are CUDA device pointers; "host" pointers are CPU memory.
+ * - BF16 tensors are passed as uint16_t bit patterns.  All matrices are row-major.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *   compute call is asynchronous on that stream, launches kernels only, allocates nothing
+ *   and never synchronises or copies device -> host.
+ * - The caller owns every buffer.  The only calls that allocate are
+ *   moe_expert_table_create (once, at load) and moe_expert_table_destroy (frees it).
+ * - Every call returns a moe_status.  Host-side argument checks run before any launch; a
+ *   call that returns an error has launched nothing.  Problems only the GPU can see (an
+ *   expert id out of range, inconsistent offsets, a pipeline wait that timed out) set a
+ *   sticky device error word that moe_get_device_error() reads and clears.  Nothing aborts
+ *   the process, nothing traps the GPU.
+ */
+#ifndef MOE_PREFILL_H
+#define MOE_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* NULL where a buffer is required, negative size, ...  */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* a shape outside what the kernels support (see calls) */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  MOE_ERR_CUDA = 4,               /* a CUDA runtime call failed (launch, copy, attribute) */
+  MOE_ERR_DEVICE = 5,             /* moe_get_device_error: a device-side check fired      */
+  MOE_ERR_NOT_BUILT_FOR_DEVICE = 6/* the current GPU is not sm_103 / sm_100 family        */
+} moe_status;
+
+/* device error codes (value of *code from moe_get_device_error) */
+#define MOE_DEVERR_NONE 0
+#define MOE_DEVERR_BAD_EXPERT_ID 1   /* an id outside [-1, E) reached the sort; treated as -1 */
+#define MOE_DEVERR_BAD_OFFSETS 2     /* expert_offsets not monotone or past R; GEMM skipped  */
+#define MOE_DEVERR_TIMEOUT 3         /* a pipeline wait in a GEMM kernel exceeded its limit  */
+#define MOE_DEVERR_NAN_LOGIT 4       /* a NaN routing logit; it is ranked below every number */
+#define MOE_DEVERR_BAD_GATHER 5      /* a gather index outside [0, a_rows); row 0 was read */
+
+/* output element type of the grouped GEMM */
+#define MOE_DTYPE_BF16 0
+#define MOE_DTYPE_F32 1
+
+/* ---------------------------------------------------------------- NVFP4 expert tables */
+/*
+ * One projection (gate/up, or down) of all experts, indexed by GLOBAL expert id.
+ * Per expert e ("Module forward_prefill_gemm", table "Layout compatibility"):
+ *   packed[e]  device, uint8 [N, K/2]: row n, byte k/2 holds logical k; even k is the low
+ *              nibble, odd k the high nibble; each nibble is an E2M1 code.
+ *   scales[e]  device, uint8 [N, K/16]: E4M3 block scale of (n, k) at [n, k/16].
+ *   scale2[e]  FP32 per-expert scale.
+ * The dequantised weight is bf16( fp32( fp32(E2M1[nibble] * e4m3) * scale2 ) ), i.e. the
+ * value the pages' grouped kernel stages ("What is NOT bit-identical", item 2).
+ * packed[e] == NULL marks an absent (remote, expert-parallel) expert: its rows are never
+ * read; the GEMMs write zeros to its output rows, which is what the pages' zeroed
+ * routed-output buffer left there.
+ *
+ * Requirements: 1 <= E <= 1024, N % 8 == 0, 8 <= N, K % 256 == 0, K >= 256; every non-NULL
+ * packed[e] and scales[e] 16-byte aligned.  The weights are NOT copied: the table refers to
+ * the caller's buffers, which must outlive it.
+ *
+ * packed, scales: host arrays of E device pointers.  scale2: host array of E floats.
+ * On success *out receives an opaque table (device memory for the per-expert TMA
+ * descriptors, pointers and scale2 values, allocated here, once).
+ */
+typedef struct moe_expert_table moe_expert_table;
+
+int moe_expert_table_create(const void* const* packed, const void* const* scales, const float* scale2,
+                            int E, int N, int K, moe_expert_table** out);
+/* Frees a table (synchronises the device first). NULL is accepted. */
+int moe_expert_table_destroy(moe_expert_table* table);
+/* Reads back E, N, K of a table (host only). */
+int moe_expert_table_shape(const moe_expert_table* table, int* E, int* N, int* K);
+
+/* ---------------------------------------------------------------- routing */
+/*
+ * Router logits: logits[t, e] = sum_h x[t, h] * w_router[e, h], BF16 inputs, FP32
+ * accumulation and output ("glm5next_mlp/forward.rs", forward_moe: the router writes
+ * [rows, num_experts] F32 logits).
+ *   x        device BF16 [T, H]
+ *   w_router device BF16 [E, H]
+ *   logits   device FP32 [T, E] (output)
+ * Requirements: T >= 1, 1 <= E <= 1024, H % 8 == 0, x and w_router 16-byte aligned.
+ */
+int moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, float* logits,
+                      void* stream);
+
+/*
+ * Top-k routing, one launch for all rows ("glm5next_mlp/forward.rs", forward_moe: one
+ * glm5next_router_topk launch with router_bias, routed_scale and renormalize):
+ *   key[t, e] = logits[t, e] (+ bias[e], FP32 add, when bias != NULL; bias only selects);
+ *   ids[t, :] = the k experts of largest key, in descending key order, ties to the lower id;
+ *   wts[t, s] = softmax of the k selected (unbiased) logits * routed_scale when renormalize,
+ *               else the full-E softmax value * routed_scale.
+ *   logits device FP32 [T, E]; bias device FP32 [E] or NULL;
+ *   ids    device int32 [T, k] (output); wts device FP32 [T, k] (output).
+ * Requirements: T >= 1, 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * A NaN logit ranks below every number and sets MOE_DEVERR_NAN_LOGIT.
+ */
+int moe_route_topk(const float* logits, const float* bias, int T, int E, int k, int renormalize,
+                   float routed_scale, int32_t* ids, float* wts, void* stream);
+
+/* ---------------------------------------------------------------- expert sort */
+/*
+ * Stable counting sort of the R = T*k routed slots by expert id ("glm5next_mlp/forward.rs"
+ * (metrale), Glm5NextMlpWorkspace fields sorted_token_ids, sorted_expert_ids,
+ * expert_offsets, token_to_perm).  Slot i = t*k + s with id e goes to sorted row
+ *   p = expert_offsets[e] + (number of earlier slots i' < i with the same id);
+ *   sorted_token_ids[p] = t (the original token), sorted_expert_ids[p] = e,
+ *   token_to_perm[i] = p, expert_offsets[0] = 0, expert_offsets[E] = number of valid slots.
+ * A slot with id -1 (the pages' "slot unfilled" sentinel) goes to a tail after
+ * expert_offsets[E] (sorted_expert_ids = -1) and gets token_to_perm = -1.  An id outside
+ * [-1, E) is treated as -1 and sets MOE_DEVERR_BAD_EXPERT_ID.
+ *   ids              device int32 [T, k]
+ *   sorted_token_ids device int32 [T*k] (output)
+ *   sorted_expert_ids device int32 [T*k] (output)
+ *   expert_offsets   device int32 [E+1] (output)
+ *   token_to_perm    device int32 [T*k] (output)
+ *   ws, ws_bytes     device scratch of at least moe_sort_workspace_bytes(T, k, E) bytes
+ * Requirements: T >= 1, 1 <= k <= 32, 1 <= E <= 1024, T*k < 2^31.
+ */
+size_t moe_sort_workspace_bytes(int T, int k, int E);
+int moe_sort_by_expert(const int32_t* ids, int T, int k, int E, int32_t* sorted_token_ids,
+                       int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- grouped W4A16 GEMM */
+/*
+ * One launch for all experts ("Module forward_prefill_gemm", "What this replaces"):
+ *   C[p, n] = sum_k A[g(p), k] * Wdq_e[n, k]   for every sorted row p in
+ *   [expert_offsets[e], expert_offsets[e+1]), n < N,
+ * where g(p) = gather_ids[p] (the in-kernel A gather through sorted_token_ids) or p when
+ * gather_ids is NULL, and Wdq_e is expert e's dequantised BF16 weight (see the table).
+ * BF16 operands, FP32 accumulation; C is BF16 (rounded to nearest even) or FP32.
+ * Rows of absent experts (packed NULL) are written as zeros; rows past expert_offsets[E]
+ * are not touched.
+ *   A            device BF16 [a_rows, lda], K = W->K columns used, lda >= K
+ *   gather_ids   device int32 [R] or NULL; every value must be in [0, a_rows)
+ *   W            expert table (E, N, K)
+ *   expert_offsets device int32 [E+1], non-decreasing, expert_offsets[E] <= R
+ *   C            device [R, ldc] of c_dtype (output), ldc >= N
+ * Requirements: lda % 8 == 0, ldc % 8 == 0, A and C 16-byte aligned, R >= 1.
+ * The kernel reads expert_offsets on the device: no host round trip, graph-capturable.
+ */
+int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                           const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
+                           int c_dtype, void* stream);
+
+/*
+ * Dequantise one expert's NVFP4 weight to a dense BF16 matrix with the grouped GEMM's own
+ * device routine (for inspection and tests; the GEMMs never materialise this matrix):
+ *   out[n, k] = bf16( fp32( fp32(E2M1[nibble(n, k)] * e4m3(scales[n, k/16])) * scale2 ) ).
+ *   packed device uint8 [N, K/2]; scales device uint8 [N, K/16]; out device BF16 [N, K].
+ * Requirements: N >= 1, K % 64 == 0, packed and out 16-byte aligned, scales 4-byte aligned.
+ */
+int moe_dequant_nvfp4(const void* packed, const void* scales, float scale2, int N, int K, uint16_t* out,
+                      void* stream);
+
+/* ---------------------------------------------------------------- activation and combine */
+/*
+ * Clamped SwiGLU ("glm5next_mlp/forward.rs", swiglu / swiglu_rows):
+ *   out[r, j] = silu(min(gate[r, j], L)) * clamp(up[r, j], -L, L),  silu(z) = z / (1 + e^-z),
+ * FP32 math, BF16 in and out.  gate/up/out are device BF16 with row strides ld_in/ld_out
+ * (elements); the fused gate/up GEMM output [R, 2I] is used as gate = G, up = G + I.
+ * Requirements: rows >= 0, width >= 1, width % 8 == 0, ld_in % 8 == 0, ld_out % 8 == 0,
+ * 16-byte aligned pointers.
+ */
+int moe_swiglu_clamp(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in,
+                     uint16_t* out, int64_t ld_out, float limit, void* stream);
+
+/*
+ * Routing-weighted combine back to token order ("glm5next_mlp/forward.rs" (metrale),
+ * forward_moe: glm5next_moe_combine_indexed):
+ *   out[t, h] = sum_{s<k} wts[t, s] * Y[token_to_perm[t, s], h]  (+ shared_out[t, h]),
+ * FP32 accumulation in slot order, BF16 output.  A slot with token_to_perm = -1 adds zero.
+ *   Y device BF16 [*, H] expert-sorted; token_to_perm device int32 [T, k];
+ *   wts device FP32 [T, k]; shared_out device BF16 [T, H] or NULL; out device BF16 [T, H].
+ * Requirements: T >= 1, 1 <= k <= 32, H % 8 == 0, 16-byte aligned BF16 pointers.
+ */
+int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const float* wts,
+                        const uint16_t* shared_out, int T, int k, int H, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------- fused forward */
+typedef struct {
+  int hidden;             /* H */
+  int moe_intermediate;   /* I (gate/up table has N = 2I: rows 0..I-1 gate, I..2I-1 up) */
+  int num_experts;        /* E */
+  int top_k;              /* k */
+  float swiglu_limit;     /* L, e.g. 7.0 */
+  int renormalize;        /* 1: renormalise the top-k weights */
+  float routed_scale;     /* multiplier of the routing weights, e.g. 1.0 */
+} moe_prefill_config;
+
+/* Workspace bytes for moe_prefill_forward with up to max_rows rows (0 on a bad config). */
+size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
+
+/* Number of stage events moe_prefill_forward records when stage_events != NULL. */
+#define MOE_FWD_NUM_EVENTS 8
+
+/*
+ * The whole routed-MoE prefill site for T rows ("glm5next_mlp/forward.rs" (metrale),
+ * forward_moe, grouped-prefill arm): router logits (when w_router != NULL) -> top-k ->
+ * expert sort -> grouped gate/up GEMM with the A gather -> SwiGLU -> grouped down GEMM ->
+ * indexed combine.  No host round trip (the pages read expert_offsets back once; here the
+ * GEMMs schedule their tiles from expert_offsets on the device), so the call can be captured
+ * in a CUDA graph.
+ *   x          device BF16 [T, H]
+ *   w_router   device BF16 [E, H] or NULL
+ *   logits_in  device FP32 [T, E] or NULL  (exactly one of w_router / logits_in)
+ *   router_bias device FP32 [E] or NULL (selection only)
+ *   w_gate_up  table with E = cfg E, N = 2I, K = H;  w_down: E, N = H, K = I
+ *   ws, ws_bytes device workspace >= moe_workspace_bytes(cfg, T), 256-byte aligned.  Its
+ *              contents after the call: logits, ids, wts, the sort arrays, G, act, Y, at the
+ *              offsets moe_workspace_layout reports.
+ *   out        device BF16 [T, H]
+ *   stage_events NULL, or a host array of MOE_FWD_NUM_EVENTS cudaEvent_t (as void*) recorded
+ *              on `stream` before the first stage and after each of the 7 stages (router,
+ *              top-k, sort count, sort scatter, gate/up GEMM, SwiGLU, down GEMM, combine
+ *              -> events 0..7 bracket them; a skipped router records event 1 = event 0).
+ */
+int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
+                        const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,
+                        const moe_expert_table* w_down, void* ws, size_t ws_bytes, uint16_t* out,
+                        void* const* stage_events, void* stream);
+
+/* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection). */
+typedef struct {
+  size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, G,
+      act, Y, total;
+} moe_workspace_layout_t;
+int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_workspace_layout_t* layout);
+
+/* ---------------------------------------------------------------- errors */
+/*
+ * Synchronises `stream`, returns the sticky device error word of the current device in
+ * *code (MOE_DEVERR_*) and clears it.  Returns MOE_ERR_DEVICE when *code != 0.
+ * For tests and debugging: it blocks the host.
+ */
+int moe_get_device_error(void* stream, int* code);
+
+/* Human-readable name of a moe_status. */
+const char* moe_status_string(int status);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PREFILL_H */

@@ -1,0 +1,444 @@
+// api.cu -- the C ABI (include/moe_prefill.h): argument checks, NVFP4 expert tables (per-expert
+// TMA descriptors built once at load), workspace layout, launches, and the fused forward.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+struct moe_expert_table {
+  int E, N, K;
+  int device;
+  CUtensorMap* d_maps;    // [E][2]
+  const void** d_packed;  // [E]
+  float* d_scale2;        // [E]
+};
+
+namespace moe {
+
+__device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_addr[kMaxDevices] = {nullptr};
+int g_sm_count[kMaxDevices] = {0};
+int g_arch_ok[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 not sm_103
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+// Once per device: the compute capability check, the SM count and the error word address.
+int ensure_device() {
+  const int d = current_device();
+  if (d < 0) return MOE_ERR_CUDA;
+  if (g_arch_ok[d] == 1) return MOE_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_arch_ok[d] == 0) {
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, d) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!(p.major == 10 && p.minor == 3)) {
+      g_arch_ok[d] = -1;
+    } else {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return MOE_ERR_CUDA;
+      g_err_addr[d] = static_cast<int*>(addr);
+      g_sm_count[d] = p.multiProcessorCount;
+      g_arch_ok[d] = 1;
+    }
+  }
+  return g_arch_ok[d] == 1 ? MOE_OK : MOE_ERR_NOT_BUILT_FOR_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+int device_sm_count() {
+  const int d = current_device();
+  return d < 0 ? 0 : g_sm_count[d];
+}
+
+int* device_error_word() {
+  const int d = current_device();
+  return d < 0 ? nullptr : g_err_addr[d];
+}
+
+int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box, const cuuint32_t* elem_strides,
+                CUtensorMapSwizzle swizzle) {
+  if (g_encode == nullptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MOE_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const CUresult r = g_encode(map, dtype, (cuuint32_t)rank, base, dims, strides_bytes, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ==================================================================================================
+// C ABI
+
+extern "C" {
+
+const char* moe_version(void) { return "moe_prefill_nvfp4_gb300 0.1 (sm_103a)"; }
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    case MOE_ERR_NOT_BUILT_FOR_DEVICE: return "MOE_ERR_NOT_BUILT_FOR_DEVICE";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+// ------------------------------------------------------------------------------------------ tables
+
+int moe_expert_table_create(const void* const* packed, const void* const* scales, const float* scale2, int E, int N,
+                            int K, moe_expert_table** out) {
+  if (out == nullptr || packed == nullptr || scales == nullptr || scale2 == nullptr) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (E < 1 || E > 1024 || N < 8 || N % 8 != 0 || K < 256 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)N * K / 2 > (1ll << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int any = 0;
+  for (int e = 0; e < E; ++e) {
+    if (packed[e] == nullptr) continue;
+    if (scales[e] == nullptr || !aligned16(packed[e]) || !aligned16(scales[e])) return MOE_ERR_INVALID_ARG;
+    any = 1;
+  }
+  if (!any) return MOE_ERR_INVALID_ARG;
+  int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+
+  std::vector<CUtensorMap> maps(2 * (size_t)E);
+  std::memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
+  for (int e = 0; e < E; ++e) {
+    if (packed[e] == nullptr) continue;
+    const cuuint32_t estr[2] = {1, 1};
+    {  // packed nibbles [N, K/2] bytes: box 128 B x 128 rows, 128-byte swizzle
+      const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+      const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+      const cuuint32_t box[2] = {128, 128};
+      rc = encode_tmap(&maps[2 * e], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(packed[e]), dims, strides,
+                       box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != MOE_OK) return rc;
+    }
+    {  // E4M3 scales [N, K/16] bytes: box 16 B x 128 rows
+      const cuuint64_t dims[2] = {(cuuint64_t)K / 16, (cuuint64_t)N};
+      const cuuint64_t strides[1] = {(cuuint64_t)K / 16};
+      const cuuint32_t box[2] = {16, 128};
+      rc = encode_tmap(&maps[2 * e + 1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales[e]), dims, strides,
+                       box, estr, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != MOE_OK) return rc;
+    }
+  }
+  moe_expert_table* t = new moe_expert_table();
+  t->E = E;
+  t->N = N;
+  t->K = K;
+  t->device = current_device();
+  t->d_maps = nullptr;
+  t->d_packed = nullptr;
+  t->d_scale2 = nullptr;
+  bool ok = cudaMalloc(&t->d_maps, maps.size() * sizeof(CUtensorMap)) == cudaSuccess &&
+            cudaMalloc(&t->d_packed, (size_t)E * sizeof(void*)) == cudaSuccess &&
+            cudaMalloc(&t->d_scale2, (size_t)E * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMemcpy(t->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(t->d_packed, packed, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(t->d_scale2, scale2, (size_t)E * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!ok) {
+    moe_expert_table_destroy(t);
+    return MOE_ERR_CUDA;
+  }
+  *out = t;
+  return MOE_OK;
+}
+
+int moe_expert_table_destroy(moe_expert_table* t) {
+  if (t == nullptr) return MOE_OK;
+  cudaDeviceSynchronize();
+  cudaFree(t->d_maps);
+  cudaFree(t->d_packed);
+  cudaFree(t->d_scale2);
+  delete t;
+  return MOE_OK;
+}
+
+int moe_expert_table_shape(const moe_expert_table* t, int* E, int* N, int* K) {
+  if (t == nullptr) return MOE_ERR_INVALID_ARG;
+  if (E) *E = t->E;
+  if (N) *N = t->N;
+  if (K) *K = t->K;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------------------------------ routing
+
+int moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, float* logits, void* stream) {
+  if (x == nullptr || w_router == nullptr || logits == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 1024 || H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w_router) || (reinterpret_cast<uintptr_t>(logits) & 3u)) return MOE_ERR_INVALID_ARG;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return router_logits_launch(x, w_router, T, H, E, logits, as_stream(stream));
+}
+
+int moe_route_topk(const float* logits, const float* bias, int T, int E, int k, int renormalize, float routed_scale,
+                   int32_t* ids, float* wts, void* stream) {
+  if (logits == nullptr || ids == nullptr || wts == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return route_topk_launch(logits, bias, T, E, k, renormalize, routed_scale, ids, wts, device_error_word(),
+                           as_stream(stream));
+}
+
+// ------------------------------------------------------------------------------------------ sort
+
+size_t moe_sort_workspace_bytes(int T, int k, int E) {
+  if (T < 1 || k < 1 || E < 1 || E > 1024 || (long long)T * k >= (1ll << 31)) return 0;
+  return sort_scratch_bytes(T * k, E);
+}
+
+int moe_sort_by_expert(const int32_t* ids, int T, int k, int E, int32_t* sorted_token_ids, int32_t* sorted_expert_ids,
+                       int32_t* expert_offsets, int32_t* token_to_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (!ids || !sorted_token_ids || !sorted_expert_ids || !expert_offsets || !token_to_perm || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > 32 || E < 1 || E > 1024 || (long long)T * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < moe_sort_workspace_bytes(T, k, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  const int R = T * k;
+  int32_t* cnt = static_cast<int32_t*>(ws);
+  rc = sort_count_launch(ids, R, E, cnt, device_error_word(), as_stream(stream));
+  if (rc != MOE_OK) return rc;
+  return sort_scatter_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
+                             as_stream(stream));
+}
+
+// ------------------------------------------------------------------------------------------ GEMM
+
+static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids, const moe_expert_table* W,
+                        const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st) {
+  if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (a_rows < 1 || R < 1 || lda < W->K || lda % 8 != 0 || ldc < W->N || ldc % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(C)) return MOE_ERR_INVALID_ARG;
+  int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  if (current_device() != W->device) return MOE_ERR_INVALID_ARG;
+  GemmArgs a;
+  a.wmaps = W->d_maps;
+  a.packed = W->d_packed;
+  a.scale2 = W->d_scale2;
+  a.gather = gather_ids;
+  a.offsets = expert_offsets;
+  a.C = C;
+  a.E = W->E;
+  a.N = W->N;
+  a.K = W->K;
+  a.R = R;
+  a.a_rows = a_rows;
+  a.ldc = ldc;
+  a.c_dtype = c_dtype;
+  a.err = device_error_word();
+  return grouped_gemm_launch(a, A, a_rows, lda, st);
+}
+
+int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                           const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
+                           int c_dtype, void* stream) {
+  return gemm_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, C, ldc, c_dtype, as_stream(stream));
+}
+
+int moe_dequant_nvfp4(const void* packed, const void* scales, float scale2, int N, int K, uint16_t* out,
+                      void* stream) {
+  if (packed == nullptr || scales == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (N < 1 || K < 64 || K % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(scales) & 3u) || (K / 16) % 4 != 0)
+    return MOE_ERR_INVALID_ARG;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return dequant_launch(static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(scales), scale2, N, K, out,
+                        as_stream(stream));
+}
+
+// ------------------------------------------------------------------------------------------ elementwise
+
+int moe_swiglu_clamp(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in,
+                     uint16_t* out, int64_t ld_out, float limit, void* stream) {
+  if (gate == nullptr || up == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || width < 1 || width % 8 != 0 || ld_in % 8 != 0 || ld_out % 8 != 0 || ld_in < width || ld_out < width)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return swiglu_launch(gate, up, rows, width, ld_in, out, ld_out, limit, as_stream(stream));
+}
+
+int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const float* wts, const uint16_t* shared_out,
+                        int T, int k, int H, uint16_t* out, void* stream) {
+  if (Y == nullptr || token_to_perm == nullptr || wts == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > 32 || H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(Y) || !aligned16(out) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return combine_launch(Y, token_to_perm, wts, shared_out, T, k, H, out, as_stream(stream));
+}
+
+// ------------------------------------------------------------------------------------------ forward
+
+static bool cfg_ok(const moe_prefill_config* c) {
+  return c != nullptr && c->hidden >= 256 && c->hidden % 256 == 0 && c->moe_intermediate >= 256 &&
+         c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 1024 && c->top_k >= 1 &&
+         c->top_k <= 32 && c->top_k <= c->num_experts;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspace_layout_t* L) {
+  if (L == nullptr || !cfg_ok(c) || max_rows < 1) return MOE_ERR_INVALID_ARG;
+  const size_t T = (size_t)max_rows, E = (size_t)c->num_experts, k = (size_t)c->top_k;
+  const size_t H = (size_t)c->hidden, I = (size_t)c->moe_intermediate, R = T * k;
+  if (R >= (1ull << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L->logits = take(T * E * 4);
+  L->ids = take(R * 4);
+  L->wts = take(R * 4);
+  L->sorted_token_ids = take(R * 4);
+  L->sorted_expert_ids = take(R * 4);
+  L->expert_offsets = take((E + 1) * 4);
+  L->token_to_perm = take(R * 4);
+  L->sort_scratch = take(sort_scratch_bytes((int)R, (int)E));
+  L->G = take(R * 2 * I * 2);
+  L->act = take(R * I * 2);
+  L->Y = take(R * H * 2);
+  L->total = o;
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows) {
+  moe_workspace_layout_t L;
+  return moe_workspace_layout(cfg, max_rows, &L) == MOE_OK ? L.total : 0;
+}
+
+int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
+                        const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,
+                        const moe_expert_table* w_down, void* ws, size_t ws_bytes, uint16_t* out,
+                        void* const* stage_events, void* stream) {
+  if (!cfg_ok(cfg) || x == nullptr || out == nullptr || ws == nullptr || w_gate_up == nullptr || w_down == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if ((w_router == nullptr) == (logits_in == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (T < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int H = cfg->hidden, I = cfg->moe_intermediate, E = cfg->num_experts, k = cfg->top_k;
+  if (w_gate_up->E != E || w_gate_up->N != 2 * I || w_gate_up->K != H) return MOE_ERR_INVALID_ARG;
+  if (w_down->E != E || w_down->N != H || w_down->K != I) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      (w_router && !aligned16(w_router)))
+    return MOE_ERR_INVALID_ARG;
+  moe_workspace_layout_t L;
+  int rc = moe_workspace_layout(cfg, T, &L);
+  if (rc != MOE_OK) return rc;
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  if (current_device() != w_gate_up->device || current_device() != w_down->device) return MOE_ERR_INVALID_ARG;
+
+  cudaStream_t st = as_stream(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* logits = reinterpret_cast<float*>(base + L.logits);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + L.ids);
+  float* wts = reinterpret_cast<float*>(base + L.wts);
+  int32_t* sti = reinterpret_cast<int32_t*>(base + L.sorted_token_ids);
+  int32_t* sei = reinterpret_cast<int32_t*>(base + L.sorted_expert_ids);
+  int32_t* off = reinterpret_cast<int32_t*>(base + L.expert_offsets);
+  int32_t* t2p = reinterpret_cast<int32_t*>(base + L.token_to_perm);
+  int32_t* cnt = reinterpret_cast<int32_t*>(base + L.sort_scratch);
+  uint16_t* G = reinterpret_cast<uint16_t*>(base + L.G);
+  uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
+  uint16_t* Y = reinterpret_cast<uint16_t*>(base + L.Y);
+  const int R = T * k;
+  int* err = device_error_word();
+  auto ev = [&](int i) {
+    if (stage_events && stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
+  };
+
+  ev(0);
+  const float* lg = logits_in;
+  if (w_router) {
+    rc = router_logits_launch(x, w_router, T, H, E, logits, st);
+    if (rc != MOE_OK) return rc;
+    lg = logits;
+  }
+  ev(1);
+  if ((rc = route_topk_launch(lg, router_bias, T, E, k, cfg->renormalize, cfg->routed_scale, ids, wts, err, st)) !=
+      MOE_OK)
+    return rc;
+  ev(2);
+  if ((rc = sort_count_launch(ids, R, E, cnt, err, st)) != MOE_OK) return rc;
+  if ((rc = sort_scatter_launch(ids, R, k, E, cnt, sti, sei, off, t2p, st)) != MOE_OK) return rc;
+  ev(3);
+  if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+  ev(4);
+  if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
+  ev(5);
+  if ((rc = gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+  ev(6);
+  if ((rc = combine_launch(Y, t2p, wts, nullptr, T, k, H, out, st)) != MOE_OK) return rc;
+  ev(7);
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------------------------------ errors
+
+int moe_get_device_error(void* stream, int* code) {
+  if (code == nullptr) return MOE_ERR_INVALID_ARG;
+  *code = 0;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+}  // extern "C"

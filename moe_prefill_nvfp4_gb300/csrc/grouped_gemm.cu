@@ -1,0 +1,440 @@
+// grouped_gemm.cu -- persistent grouped W4A16 GEMM for sm_103a (tcgen05 + TMA + TMEM).
+//
+// One launch covers every expert ("Module forward_prefill_gemm", "What this replaces": one
+// launch for all experts, an expert_offsets prefix sum, the A gather through
+// sorted_token_ids inside the kernel).  For each expert e and sorted row p in
+// [off[e], off[e+1]):  C[p, n] = sum_k A[g(p), k] * Wdq_e[n, k].
+//
+// Work decomposition ("swap AB"): a tile is (expert e, 128 weight rows n0..n0+127, up to
+// BN_MAX of the expert's rows).  The 128 weight rows are the MMA's M operand and live in
+// TENSOR MEMORY: dequantisation warps turn the TMA-loaded NVFP4 bytes into BF16 and write them
+// with tcgen05.st straight into TMEM (no shared-memory round trip for A).  The expert's rows
+// (tokens) are the MMA's N operand (16..256 wide, padded to 16), gathered by TMA gather4 into
+// 128-byte-swizzled shared memory.  FP32 accumulators stay in TMEM until the epilogue.
+//
+// Tile order is (expert, n-block, token-block) with the token-block fastest, so the CTAs that
+// share one expert's weights run at the same time and the repeats hit L2: each expert's
+// packed weights and scales are read from HBM once per launch.  The static round-robin tile
+// walk is the persistent scheduler: it is driven by expert_offsets on the device, balances
+// skew by splitting heavy experts into many token blocks, and needs no host round trip.
+//
+// Warp roles (15 warps):
+//   0-3   epilogue: TMEM -> registers -> BF16/FP32 -> shared staging -> 16-byte global stores
+//   4-11  dequantisation, two warpgroups taking alternate 64-k sub-stages
+//   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B])
+//   13    activation producer (TMA gather4, 4 rows per instruction)
+//   14    MMA issuer (one thread) and TMEM owner
+// Every pipeline wait is bounded: on a timeout the CTA records MOE_DEVERR_TIMEOUT, drains its
+// in-flight copies and MMAs, frees TMEM and exits.
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;      // weight rows per tile = MMA M = TMEM lanes
+constexpr int BKW = 256;     // k per weight stage (128 packed bytes per row)
+constexpr int BKA = 64;      // k per activation stage and per TMEM A stage
+constexpr int NT = 8;        // TMEM A stages (32 columns each)
+constexpr int TMEM_COLS = 512;
+constexpr int D_COL = 0;     // accumulator columns [0, 256)
+constexpr int A_COL = 256;   // A stages at [256, 512)
+constexpr int WARP_WP = 12, WARP_AP = 13, WARP_MMA = 14;
+constexpr int NUM_WARPS = 15;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int MAX_E = 1024;
+
+template <int BN_MAX_, int NA_, int NW_>
+struct Cfg {
+  static constexpr int BN_MAX = BN_MAX_;
+  static constexpr int NA = NA_;
+  static constexpr int NW = NW_;
+  static constexpr int ACT_STAGE = BN_MAX * 128;
+  static constexpr int PK_STAGE = BM * 128;
+  static constexpr int SC_STAGE = BM * 16;
+  static constexpr int EPI_WARP_BYTES = 32 * 32 * 4;
+  static constexpr int OFF_ACT = 0;
+  static constexpr int OFF_PK = OFF_ACT + NA * ACT_STAGE;
+  static constexpr int OFF_SC = OFF_PK + NW * PK_STAGE;
+  static constexpr int OFF_EPI = OFF_SC + NW * SC_STAGE;
+  static constexpr int OFF_OFFS = OFF_EPI + 4 * EPI_WARP_BYTES;
+  static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
+  static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
+  // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full d_empty drain
+  static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
+  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256, "token tile");
+  static_assert(OFF_PK % 1024 == 0 && ACT_STAGE % 1024 == 0, "swizzled buffers need 1024-byte alignment");
+};
+
+struct TileInfo {
+  int e, nb, p0, cnt, bn;
+};
+
+template <int BN_MAX>
+MOE_DEV TileInfo decode_tile(int t, const int* s_tbase, const int* s_offs, int E) {
+  int lo = 0, hi = E - 1;  // largest e in [0, E-1] with s_tbase[e] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tbase[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  const int m = s_offs[lo + 1] - s_offs[lo];
+  const int ntt = (m + BN_MAX - 1) / BN_MAX;
+  const int local = t - s_tbase[lo];
+  ti.nb = local / ntt;
+  const int tt = local - ti.nb * ntt;
+  const int chunk = (((m + ntt - 1) / ntt) + 15) & ~15;
+  ti.p0 = s_offs[lo] + tt * chunk;
+  ti.cnt = min(chunk, m - tt * chunk);
+  ti.bn = (ti.cnt + 15) & ~15;
+  return ti;
+}
+
+// lane 0 waits, the result is broadcast so the whole warp takes the same branch
+MOE_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  bool ok = true;
+  if (lane_id() == 0) ok = mbar_wait(bar, parity, abort_flag, err);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+template <class C>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap amap, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  int* s_offs = reinterpret_cast<int*>(smem + C::OFF_OFFS);
+  int* s_tbase = reinterpret_cast<int*>(smem + C::OFF_TBASE);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto w_full = [&](int s) { return bar0 + 8u * s; };
+  auto w_empty = [&](int s) { return bar0 + 8u * (C::NW + s); };
+  auto a_full = [&](int s) { return bar0 + 8u * (2 * C::NW + s); };
+  auto a_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + C::NA + s); };
+  auto t_full = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + s); };
+  auto t_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + NT + s); };
+  const uint32_t d_full = bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT);
+  const uint32_t d_empty = d_full + 8u;
+  const uint32_t drain_bar = d_full + 16u;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* s_bad = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = args.E;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NW; ++s) {
+      mbar_init(w_full(s), 1);
+      mbar_init(w_empty(s), 8);
+    }
+    for (int s = 0; s < C::NA; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
+    }
+    for (int s = 0; s < NT; ++s) {
+      mbar_init(t_full(s), 4);
+      mbar_init(t_empty(s), 1);
+    }
+    mbar_init(d_full, 1);
+    mbar_init(d_empty, 4);
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
+    tmem_relinquish();
+  }
+  for (int i = tid; i <= E; i += NUM_THREADS) s_offs[i] = args.offsets[i];
+  __syncthreads();
+
+  // tile table: expert e owns tiles [s_tbase[e], s_tbase[e+1]); absent or empty experts own none
+  const int NB = (args.N + BM - 1) / BM;
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int sum = 0;
+    bool bad = false;
+    for (int e = e0; e < e1; ++e) {
+      const int m = s_offs[e + 1] - s_offs[e];
+      if (m < 0) bad = true;
+      if (m > 0 && args.packed[e] != nullptr) sum += NB * ((m + C::BN_MAX - 1) / C::BN_MAX);
+    }
+    if (lane == 0 && (s_offs[0] != 0 || s_offs[E] > args.R || s_offs[E] < 0)) bad = true;
+    bad = __any_sync(0xffffffffu, bad);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      s_tbase[e] = bad ? 0 : run;
+      const int m = s_offs[e + 1] - s_offs[e];
+      if (m > 0 && args.packed[e] != nullptr) run += NB * ((m + C::BN_MAX - 1) / C::BN_MAX);
+    }
+    if (lane == 31) s_tbase[E] = bad ? 0 : incl;
+    if (lane == 0) *s_bad = bad ? 1 : 0;
+    if (bad && lane == 0 && blockIdx.x == 0) set_error(args.err, MOE_DEVERR_BAD_OFFSETS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = s_tbase[E];
+  const int KA = args.K / BKA;  // activation / TMEM stages per tile
+  const int KW = args.K / BKW;  // weight stages per tile
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp;
+    uint8_t* stg = smem + C::OFF_EPI + q * C::EPI_WARP_BYTES;
+    const bool f32 = args.c_dtype == MOE_DTYPE_F32;
+    const int esz = f32 ? 4 : 2;
+    // rows of absent experts are written as zeros (the pages' zeroed routed-output rows)
+    if (!*s_bad) {
+      const int chunks_per_row = args.N * esz / 16;
+      for (int e = 0; e < E; ++e) {
+        if (args.packed[e] != nullptr) continue;
+        for (int r = s_offs[e] + blockIdx.x; r < s_offs[e + 1]; r += gridDim.x) {
+          uint8_t* row = reinterpret_cast<uint8_t*>(args.C) + (size_t)r * args.ldc * esz;
+          for (int c = tid; c < chunks_per_row; c += 128) *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+      if (!warp_wait(d_full, it & 1, s_abort, args.err)) break;
+      tc_fence_after();
+      const int n0 = ti.nb * BM + q * 32;
+      for (int c0 = 0; c0 < ti.cnt; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + D_COL + c0, v);
+        tmem_wait_ld();
+        if (c0 + 32 >= ti.cnt) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(d_empty);
+        }
+        __syncwarp();
+        if (f32) {
+          float* s = reinterpret_cast<float*>(stg);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __uint_as_float(v[j]);
+        } else {
+          __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+        __syncwarp();
+        const int rows = min(32, ti.cnt - c0);
+        const int cpr = 32 * esz / 16;  // 16-byte chunks per staged row (4 bf16, 8 f32)
+        for (int c = lane; c < 32 * cpr; c += 32) {
+          const int r = c / cpr, cc = c - r * cpr;
+          const int n = n0 + cc * (16 / esz);
+          if (r < rows && n < args.N) {
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 * esz + cc * 16);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(args.C) + ((size_t)(ti.p0 + c0 + r) * args.ldc + n) * esz;
+            *reinterpret_cast<uint4*>(dst) = val;
+          }
+        }
+      }
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------------------------ dequantisation
+    const int wg = (warp - 4) >> 2;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int wi = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+      const float s2 = args.scale2[ti.e];
+      for (int ks = 0; ks < KW; ++ks, ++wi) {
+        const int s = wi % C::NW;
+        if (!warp_wait(w_full(s), (wi / C::NW) & 1, s_abort, args.err)) { ok = false; break; }
+        const uint8_t* pk = smem + C::OFF_PK + s * C::PK_STAGE + row * 128;
+        const uint4 scv = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + s * C::SC_STAGE + row * 16);
+        uint4 chunk[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int sub = wg + 2 * h;
+          chunk[2 * h] = *reinterpret_cast<const uint4*>(pk + (((2 * sub) ^ (row & 7)) << 4));
+          chunk[2 * h + 1] = *reinterpret_cast<const uint4*>(pk + (((2 * sub + 1) ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(w_empty(s));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int sub = wg + 2 * h;
+          const int tix = wi * 4 + sub;
+          const int ts = tix % NT;
+          if (!warp_wait(t_empty(ts), ((tix / NT) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t w[8] = {chunk[2 * h].x,     chunk[2 * h].y,     chunk[2 * h].z,     chunk[2 * h].w,
+                                 chunk[2 * h + 1].x, chunk[2 * h + 1].y, chunk[2 * h + 1].z, chunk[2 * h + 1].w};
+          const uint32_t sc = sub == 0 ? scv.x : sub == 1 ? scv.y : sub == 2 ? scv.z : scv.w;
+          uint32_t out[32];
+          dequant64(w, sc, s2, out);
+          tmem_st_32x32b_x32(tmem_base + lane_addr + A_COL + ts * 32, out);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(t_full(ts));
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == WARP_WP) {
+    // ------------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int wi = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+        const CUtensorMap* mp = args.wmaps + 2 * ti.e;
+        const CUtensorMap* ms = mp + 1;
+        prefetch_tmap(mp);
+        prefetch_tmap(ms);
+        for (int ks = 0; ks < KW; ++ks, ++wi) {
+          const int s = wi % C::NW;
+          if (!mbar_wait(w_empty(s), ((wi / C::NW) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(w_full(s), C::PK_STAGE + C::SC_STAGE);
+          tma_load_2d(sbase + C::OFF_PK + s * C::PK_STAGE, mp, ks * 128, ti.nb * BM, w_full(s));
+          tma_load_2d(sbase + C::OFF_SC + s * C::SC_STAGE, ms, ks * 16, ti.nb * BM, w_full(s));
+        }
+      }
+      if (!ok)
+        for (int j = max(0, wi - C::NW); j < wi; ++j) mbar_wait_drain(w_full(j % C::NW), (j / C::NW) & 1);
+    }
+  } else if (warp == WARP_AP) {
+    // ------------------------------------------------------------------ activation producer
+    int ai = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+      const int ng = ti.bn >> 2;  // gather4 ops per stage
+      constexpr int NH = (C::BN_MAX + 127) / 128;  // gather4 ops per lane per stage
+      int rows[NH * 4];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int g = lane + 32 * h;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          int p = ti.p0 + min(4 * g + r, ti.cnt - 1);
+          int src = args.gather ? args.gather[p] : p;
+          if ((unsigned)src >= (unsigned)args.a_rows) {
+            if (g < ng) set_error(args.err, MOE_DEVERR_BAD_GATHER);
+            src = 0;
+          }
+          rows[4 * h + r] = src;
+        }
+      }
+      for (int kb = 0; kb < KA; ++kb, ++ai) {
+        const int s = ai % C::NA;
+        if (!warp_wait(a_empty(s), ((ai / C::NA) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(a_full(s), ti.bn * 128);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int g = lane + 32 * h;
+          if (g < ng)
+            tma_gather4(sbase + C::OFF_ACT + s * C::ACT_STAGE + g * 512, &amap, kb * BKA, rows[4 * h],
+                        rows[4 * h + 1], rows[4 * h + 2], rows[4 * h + 3], a_full(s));
+        }
+      }
+    }
+    if (!ok && lane == 0)
+      for (int j = max(0, ai - C::NA); j < ai; ++j) mbar_wait_drain(a_full(j % C::NA), (j / C::NA) & 1);
+  } else {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int ai = 0, it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+        if (!mbar_wait(d_empty, (it & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t idesc = make_idesc_bf16(BM, ti.bn);
+        for (int kb = 0; kb < KA; ++kb, ++ai) {
+          const int s = ai % C::NA;
+          const int ts = ai % NT;
+          if (!mbar_wait(a_full(s), (ai / C::NA) & 1, s_abort, args.err)) { ok = false; break; }
+          if (!mbar_wait(t_full(ts), (ai / NT) & 1, s_abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t bsm = sbase + C::OFF_ACT + s * C::ACT_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BKA / 16; ++kk)
+            mma_bf16_ts(tmem_base + D_COL, tmem_base + A_COL + ts * 32 + kk * 8, make_sdesc_sw128(bsm + kk * 32),
+                        idesc, (kb | kk) != 0);
+          mma_commit(a_empty(s));
+          mma_commit(t_empty(ts));
+        }
+        if (ok) mma_commit(d_full);
+      }
+      if (!ok) {
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+using CfgLarge = Cfg<256, 3, 4>;
+
+}  // namespace gg
+
+// ------------------------------------------------------------------------------------------------
+// host side
+
+int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda, cudaStream_t stream) {
+  using C = gg::CfgLarge;
+  CUtensorMap amap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)a_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    int rc = encode_tmap(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box, estr,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != MOE_OK) return rc;
+  }
+  static int configured_device = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (configured_device != dev) {
+    if (cudaFuncSetAttribute(gg::grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured_device = dev;
+  }
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  const long long nb = (args.N + gg::BM - 1) / gg::BM;
+  const long long max_tiles = nb * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(nsm, max_tiles));
+  gg::grouped_gemm_kernel<C><<<grid, gg::NUM_THREADS, C::SMEM_ALLOC, stream>>>(amap, args);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

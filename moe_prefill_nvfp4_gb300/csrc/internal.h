@@ -1,0 +1,51 @@
+// internal.h -- declarations shared between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_prefill.h"
+
+namespace moe {
+
+// Arguments of the grouped W4A16 GEMM kernel (the activation tensor map is passed separately as
+// a __grid_constant__ parameter).
+struct GemmArgs {
+  const CUtensorMap* wmaps;   // device [E][2]: packed [N, K/2] map, scales [N, K/16] map
+  const void* const* packed;  // device [E]: packed pointers (NULL = absent expert)
+  const float* scale2;        // device [E]
+  const int32_t* gather;      // device [R] or NULL (identity)
+  const int32_t* offsets;     // device [E+1]
+  void* C;
+  int E, N, K, R, a_rows, ldc, c_dtype;
+  int* err;                   // device error word
+};
+
+// Host: encode a tiled tensor map through the driver entry point (no libcuda link needed).
+int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box, const cuuint32_t* elem_strides,
+                CUtensorMapSwizzle swizzle);
+int device_sm_count();
+int* device_error_word();  // device address of the current device's error word
+
+int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda, cudaStream_t stream);
+
+// SIMT kernels (small_kernels.cu)
+int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st);
+int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
+                      int32_t* ids, float* wts, int* err, cudaStream_t st);
+int sort_segments(int R, int E);
+size_t sort_scratch_bytes(int R, int E);
+int sort_count_launch(const int32_t* ids, int R, int E, int32_t* cnt, int* err, cudaStream_t st);
+int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* cnt, int32_t* sorted_token_ids,
+                        int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
+                        cudaStream_t st);
+int swiglu_launch(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in, uint16_t* out,
+                  int64_t ld_out, float limit, cudaStream_t st);
+int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, const uint16_t* shared_out, int T, int k,
+                   int H, uint16_t* out, cudaStream_t st);
+int dequant_launch(const uint8_t* packed, const uint8_t* scales, float scale2, int N, int K, uint16_t* out,
+                   cudaStream_t st);
+
+}  // namespace moe

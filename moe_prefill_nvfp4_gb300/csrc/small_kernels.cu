@@ -1,0 +1,392 @@
+// small_kernels.cu -- the bandwidth/latency-bound steps around the two grouped GEMMs:
+// router logits, top-k routing, the stable expert sort, the clamped SwiGLU, the indexed
+// combine, and a standalone NVFP4 -> BF16 dequantisation (same device routine as the GEMM).
+//
+// Each is one launch over all rows (the pages measured per-row launches of top-k and combine
+// as pure launch overhead: "glm5next_mlp/forward.rs", forward_moe comments), with 16-byte
+// vector loads/stores on the row-major BF16 tensors and warp-level primitives (ballot,
+// shuffles) for selection, counting and the per-expert prefix.
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------------
+// router logits: logits[t, e] = sum_h x[t, h] * w[e, h]  (BF16 in, FP32 accumulate and out)
+//
+// A warp owns a 4-token x 8-expert block; lanes split h in 8-element vectors, each lane keeps
+// 32 FP32 partial sums, then a fixed xor-butterfly reduces them (deterministic order).
+
+constexpr int RL_TOK = 4, RL_EXP = 8, RL_WARPS = 4;
+
+__global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                                      const uint16_t* __restrict__ w, int T, int H,
+                                                                      int E, float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * RL_TOK;
+  const int e0 = (blockIdx.y * RL_WARPS + warp) * RL_EXP;
+  if (e0 >= E) return;
+  float acc[RL_TOK][RL_EXP];
+#pragma unroll
+  for (int i = 0; i < RL_TOK; ++i)
+#pragma unroll
+    for (int j = 0; j < RL_EXP; ++j) acc[i][j] = 0.f;
+  const int nvec = H / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    uint4 xv[RL_TOK], wv[RL_EXP];
+#pragma unroll
+    for (int i = 0; i < RL_TOK; ++i)
+      xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < RL_EXP; ++j)
+      wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + j) * H) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < RL_TOK; ++i) {
+      const uint32_t xa[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+      for (int j = 0; j < RL_EXP; ++j) {
+        const uint32_t wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+        float a = acc[i][j];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          a = fmaf(bf16_lo(xa[c]), bf16_lo(wa[c]), a);
+          a = fmaf(bf16_hi(xa[c]), bf16_hi(wa[c]), a);
+        }
+        acc[i][j] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RL_TOK; ++i)
+#pragma unroll
+    for (int j = 0; j < RL_EXP; ++j) {
+      float a = acc[i][j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == ((i * RL_EXP + j) & 31) && t0 + i < T && e0 + j < E) logits[(size_t)(t0 + i) * E + e0 + j] = a;
+    }
+}
+
+int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st) {
+  dim3 grid((T + RL_TOK - 1) / RL_TOK, (E + RL_EXP * RL_WARPS - 1) / (RL_EXP * RL_WARPS));
+  router_logits_kernel<<<grid, RL_WARPS * 32, 0, st>>>(x, w, T, H, E, logits);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// top-k routing: one warp per row; lane l holds logits of experts l, l+32, ... in registers.
+
+constexpr int TOPK_WARPS = 8;
+
+MOE_DEV bool key_better(float ka, int ea, float kb, int eb) { return ka > kb || (ka == kb && ea < eb); }
+
+template <int NPL>
+__global__ void __launch_bounds__(TOPK_WARPS * 32)
+    route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+                      int renormalize, float routed_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+                      int* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * TOPK_WARPS + warp;
+  if (row >= T) return;
+  const float* lrow = logits + (size_t)row * E;
+  float val[NPL], key[NPL];
+  bool nan_seen = false;
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    val[j] = e < E ? lrow[e] : -INFINITY;
+    key[j] = e < E ? (bias ? val[j] + bias[e] : val[j]) : -INFINITY;
+    if (e < E && (isnan(val[j]) || isnan(key[j]))) {
+      nan_seen = true;
+      key[j] = -INFINITY;
+    }
+  }
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_error(err, MOE_DEVERR_NAN_LOGIT);
+  uint32_t taken = 0;
+  int my_id = -1;
+  for (int s = 0; s < k; ++s) {
+    float bk = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u) && key_better(key[j], e, bk, be)) {
+        bk = key[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (key_better(ok, oe, bk, be)) {
+        bk = ok;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == s) my_id = be;
+  }
+  // routing weights from the unbiased logits
+  const bool mine = lane < k;
+  const float l = mine ? lrow[my_id] : -INFINITY;
+  float w;
+  if (renormalize) {
+    float m = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float ex = mine ? expf(l - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    w = ex / sum;
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) m = fmaxf(m, val[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (lane + 32 * j < E) sum += expf(val[j] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    w = mine ? expf(l - m) / sum : 0.f;
+  }
+  if (mine) {
+    ids[(size_t)row * k + lane] = my_id;
+    wts[(size_t)row * k + lane] = w * routed_scale;
+  }
+}
+
+int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
+                      int32_t* ids, float* wts, int* err, cudaStream_t st) {
+  const int grid = (T + TOPK_WARPS - 1) / TOPK_WARPS;
+  const int npl = (E + 31) / 32;
+#define MOE_TOPK_CASE(N)                                                                                  \
+  route_topk_kernel<N><<<grid, TOPK_WARPS * 32, 0, st>>>(logits, bias, T, E, k, renormalize, scale, ids, wts, err)
+  if (npl <= 1) MOE_TOPK_CASE(1);
+  else if (npl <= 2) MOE_TOPK_CASE(2);
+  else if (npl <= 4) MOE_TOPK_CASE(4);
+  else if (npl <= 8) MOE_TOPK_CASE(8);
+  else if (npl <= 16) MOE_TOPK_CASE(16);
+  else MOE_TOPK_CASE(32);
+#undef MOE_TOPK_CASE
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// stable expert sort.  The R slots are cut into S segments; warp (b, seg) handles bucket b
+// (expert b, or the tail b = E for -1 / invalid ids) in one segment:
+//   count:   cnt[b*S + seg] = number of slots of the segment in bucket b  (ballot + popc)
+//   scatter: base = sum of cnt before (b, seg) in bucket-major order = the sorted position of the
+//            bucket's first slot of the segment; the ballot prefix within each 32-slot chunk
+//            keeps flat slot order, so the sort is stable.
+
+constexpr int SORT_WARPS = 8;
+
+int sort_segments(int R, int E) {
+  const int by_size = (R + 2047) / 2048;
+  const int by_prefix = std::max(1, 2048 / (E + 1));
+  return std::max(1, std::min(64, std::min(by_size, by_prefix)));
+}
+
+size_t sort_scratch_bytes(int R, int E) { return (size_t)(E + 1) * sort_segments(R, E) * sizeof(int32_t); }
+
+MOE_DEV bool in_bucket(int id, int b, int E) { return b < E ? id == b : (id < 0 || id >= E); }
+
+__global__ void __launch_bounds__(SORT_WARPS * 32)
+    sort_count_kernel(const int32_t* __restrict__ ids, int R, int E, int S, int32_t* __restrict__ cnt, int* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = blockIdx.x * SORT_WARPS + warp;
+  if (gid >= (E + 1) * S) return;
+  const int b = gid / S, seg = gid - b * S;
+  const int L = (R + S - 1) / S;
+  const int lo = seg * L, hi = min(R, lo + L);
+  int c = 0;
+  bool bad = false;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const int id = i < hi ? ids[i] : -2;
+    if (b == E && i < hi && (id < -1 || id >= E)) bad = true;
+    c += __popc(__ballot_sync(0xffffffffu, i < hi && in_bucket(id, b, E)));
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
+  if (lane == 0) cnt[gid] = c;
+}
+
+__global__ void __launch_bounds__(SORT_WARPS * 32)
+    sort_scatter_kernel(const int32_t* __restrict__ ids, int R, int k, int E, int S, const int32_t* __restrict__ cnt,
+                        int32_t* __restrict__ sorted_token_ids, int32_t* __restrict__ sorted_expert_ids,
+                        int32_t* __restrict__ expert_offsets, int32_t* __restrict__ token_to_perm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = blockIdx.x * SORT_WARPS + warp;
+  if (gid >= (E + 1) * S) return;
+  const int b = gid / S, seg = gid - b * S;
+  int base = 0;
+  for (int i = lane; i < gid; i += 32) base += cnt[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) base += __shfl_xor_sync(0xffffffffu, base, o);
+  if (seg == 0 && lane == 0) expert_offsets[b] = base;  // b == E: number of valid slots
+  const int L = (R + S - 1) / S;
+  const int lo = seg * L, hi = min(R, lo + L);
+  const uint32_t lt = (1u << lane) - 1u;
+  int run = base;
+  for (int start = lo; start < hi; start += 32) {
+    const int i = start + lane;
+    const int id = i < hi ? ids[i] : -2;
+    const bool m = i < hi && in_bucket(id, b, E);
+    const uint32_t bal = __ballot_sync(0xffffffffu, m);
+    if (m) {
+      const int p = run + __popc(bal & lt);
+      sorted_token_ids[p] = i / k;
+      sorted_expert_ids[p] = b < E ? b : -1;
+      token_to_perm[i] = b < E ? p : -1;
+    }
+    run += __popc(bal);
+  }
+}
+
+int sort_count_launch(const int32_t* ids, int R, int E, int32_t* cnt, int* err, cudaStream_t st) {
+  const int S = sort_segments(R, E);
+  const int warps = (E + 1) * S;
+  sort_count_kernel<<<(warps + SORT_WARPS - 1) / SORT_WARPS, SORT_WARPS * 32, 0, st>>>(ids, R, E, S, cnt, err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* cnt, int32_t* sorted_token_ids,
+                        int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
+                        cudaStream_t st) {
+  const int S = sort_segments(R, E);
+  const int warps = (E + 1) * S;
+  sort_scatter_kernel<<<(warps + SORT_WARPS - 1) / SORT_WARPS, SORT_WARPS * 32, 0, st>>>(
+      ids, R, k, E, S, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// clamped SwiGLU: out = silu(min(g, L)) * clamp(u, -L, L), 8 elements per thread
+
+MOE_DEV float swiglu1(float g, float u, float L) {
+  const float gm = fminf(g, L);
+  const float uc = fminf(fmaxf(u, -L), L);
+  return gm / (1.0f + expf(-gm)) * uc;
+}
+
+__global__ void swiglu_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up, int64_t rows,
+                              int64_t width, int64_t ld_in, uint16_t* __restrict__ out, int64_t ld_out, float L) {
+  const int64_t vpr = width / 8;
+  const int64_t total = rows * vpr;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / vpr, c = (v - r * vpr) * 8;
+    const uint4 g = *reinterpret_cast<const uint4*>(gate + r * ld_in + c);
+    const uint4 u = *reinterpret_cast<const uint4*>(up + r * ld_in + c);
+    const uint32_t ga[4] = {g.x, g.y, g.z, g.w}, ua[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = pack_bf16x2(swiglu1(bf16_lo(ga[i]), bf16_lo(ua[i]), L), swiglu1(bf16_hi(ga[i]), bf16_hi(ua[i]), L));
+    *reinterpret_cast<uint4*>(out + r * ld_out + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int swiglu_launch(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in, uint16_t* out,
+                  int64_t ld_out, float limit, cudaStream_t st) {
+  const int64_t total = rows * (width / 8);
+  if (total == 0) return MOE_OK;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, (int64_t)device_sm_count() * 16);
+  swiglu_kernel<<<(int)blocks, threads, 0, st>>>(gate, up, rows, width, ld_in, out, ld_out, limit);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// indexed combine: out[t] = sum_s wts[t, s] * Y[token_to_perm[t, s]] (+ shared_out[t]), slot order
+
+constexpr int CMB_THREADS = 128;
+
+__global__ void __launch_bounds__(CMB_THREADS)
+    combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ perm, const float* __restrict__ wts,
+                   const uint16_t* __restrict__ shared_out, int k, int H, uint16_t* __restrict__ out) {
+  __shared__ int s_perm[32];
+  __shared__ float s_w[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    s_perm[threadIdx.x] = perm[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = wts[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int nvec = H / 8;
+  for (int v = threadIdx.x; v < nvec; v += CMB_THREADS) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int p = s_perm[s];
+      if (p < 0) continue;
+      const float w = s_w[s];
+      const uint4 y = *reinterpret_cast<const uint4*>(Y + (size_t)p * H + v * 8);
+      const uint32_t ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w, bf16_lo(ya[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, bf16_hi(ya[i]), acc[2 * i + 1]);
+      }
+    }
+    if (shared_out) {
+      const uint4 y = *reinterpret_cast<const uint4*>(shared_out + (size_t)t * H + v * 8);
+      const uint32_t ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += bf16_lo(ya[i]);
+        acc[2 * i + 1] += bf16_hi(ya[i]);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, const uint16_t* shared_out, int T, int k,
+                   int H, uint16_t* out, cudaStream_t st) {
+  combine_kernel<<<T, CMB_THREADS, 0, st>>>(Y, perm, wts, shared_out, k, H, out);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// standalone dequantisation: one thread per (row, 64-k chunk), the GEMM's dequant64 routine
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales, float s2, int N,
+                               int K, uint16_t* __restrict__ out) {
+  const int chunks = K / 64;
+  const int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)N * chunks) return;
+  const int n = (int)(idx / chunks), c = (int)(idx - (int64_t)n * chunks);
+  const uint4* src = reinterpret_cast<const uint4*>(packed + (size_t)n * (K / 2) + c * 32);
+  const uint4 p0 = src[0], p1 = src[1];
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(scales + (size_t)n * (K / 16) + c * 4);
+  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  uint32_t o[32];
+  dequant64(w, sc, s2, o);
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)n * K + c * 64);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
+int dequant_launch(const uint8_t* packed, const uint8_t* scales, float scale2, int N, int K, uint16_t* out,
+                   cudaStream_t st) {
+  const int64_t total = (int64_t)N * (K / 64);
+  const int threads = 128;
+  dequant_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(packed, scales, scale2, N, K, out);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

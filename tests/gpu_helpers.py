@@ -1,0 +1,89 @@
+"""Helpers of the GPU parity tests: move synthetic cases to the device, compare with the oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_prefill_nvfp4_gb300 as moe
+from moe_prefill_nvfp4_gb300.weights import upload_projection
+
+# float outputs vs the oracle, max|gpu - ref| / max|ref|
+TOL_BF16 = 4e-3  # against the variant that rounds weights and inter-stage activations to BF16
+TOL_EXACT = 1e-2  # against the exact FP32-weight variant
+
+
+def nerr(gpu, ref) -> float:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.abs(ref).max()
+    return float(np.abs(gpu - ref).max() / (den if den > 0 else 1.0))
+
+
+def bf16_dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bf16_host(t: torch.Tensor) -> np.ndarray:
+    """BF16 device tensor -> float64 numpy."""
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def upload(proj):
+    return upload_projection(proj.packed, proj.scales, proj.scale2, proj.N, proj.K)
+
+
+def make_cfg(case) -> moe.MoePrefillConfig:
+    return moe.MoePrefillConfig(hidden=case.H, moe_intermediate=case.I, num_experts=case.E, top_k=case.k,
+                                swiglu_limit=case.swiglu_limit, renormalize=case.renormalize,
+                                routed_scale=case.routed_scale)
+
+
+class DeviceBlock:
+    """A routed-MoE block case on the device, with one workspace."""
+
+    def __init__(self, case):
+        self.case = case
+        self.x = bf16_dev(case.x)
+        self.router_w = bf16_dev(case.router_w) if case.router_w is not None else None
+        self.logits = torch.from_numpy(case.logits).cuda() if case.logits is not None else None
+        self.gu = upload(case.gate_up)
+        self.dn = upload(case.down)
+        self.cfg = make_cfg(case)
+        self.layout = moe.moe_workspace_layout(self.cfg, case.T)
+        self.ws = torch.empty(self.layout.total, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(case.T, case.H, dtype=torch.bfloat16, device="cuda")
+
+    def forward(self, stream=None):
+        return moe.moe_prefill_forward(self.cfg, self.x, self.gu.table, self.dn.table, self.ws, w_router=self.router_w,
+                                       logits=self.logits, out=self.out, stream=stream)
+
+    def ws_view(self, name: str, dtype: torch.dtype, shape) -> torch.Tensor:
+        off = getattr(self.layout, name)
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        return self.ws[off:off + n].view(dtype).view(*shape)
+
+    def stages(self):
+        c = self.case
+        R = c.T * c.k
+        return dict(
+            logits=self.ws_view("logits", torch.float32, (c.T, c.E)).cpu().numpy(),
+            ids=self.ws_view("ids", torch.int32, (c.T, c.k)).cpu().numpy(),
+            wts=self.ws_view("wts", torch.float32, (c.T, c.k)).cpu().numpy(),
+            sorted_token_ids=self.ws_view("sorted_token_ids", torch.int32, (R,)).cpu().numpy(),
+            sorted_expert_ids=self.ws_view("sorted_expert_ids", torch.int32, (R,)).cpu().numpy(),
+            expert_offsets=self.ws_view("expert_offsets", torch.int32, (c.E + 1,)).cpu().numpy(),
+            token_to_perm=self.ws_view("token_to_perm", torch.int32, (c.T, c.k)).cpu().numpy(),
+            G=bf16_host(self.ws_view("G", torch.bfloat16, (R, 2 * c.I))),
+            act=bf16_host(self.ws_view("act", torch.bfloat16, (R, c.I))),
+            Y=bf16_host(self.ws_view("Y", torch.bfloat16, (R, c.H))),
+            out=bf16_host(self.out),
+        )
+
+    def close(self):
+        self.gu.close()
+        self.dn.close()

@@ -169,6 +169,10 @@ def run_gpu(args):
         raise RuntimeError("device error during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(args.steps)]
+    for row in evs:  # torch creates the CUDA event on first record; the library records it afterwards
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if ws_n > 1:
         dist.barrier()

@@ -8,7 +8,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/moe_prefill.h"
+#include "moe_prefill.h"
 
 #define MOE_DEV __device__ __forceinline__
 
@@ -58,9 +58,22 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or about
+// `hint_ns` pass, instead of re-issuing the poll (idle roles then take no issue slots).
+MOE_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Upper bound of any single pipeline wait.  A wait that exceeds it means the pipeline is
 // broken; the kernel records MOE_DEVERR_TIMEOUT and unwinds instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kSleepHintNs = 20000u;         // 20 us per suspended poll
 
 // Waits for the phase of `parity` to complete.  Returns false when the CTA-wide abort flag is
 // raised (by this or another role) or when the wait limit is exceeded (then it raises the
@@ -68,15 +81,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        set_error(err, MOE_DEVERR_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
     }
   }
 }
@@ -85,7 +96,7 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, 
 MOE_DEV bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
@@ -123,6 +134,54 @@ MOE_DEV void tma_gather4(uint32_t dst, const void* tmap, int x, int y0, int y1, 
       : "memory");
 }
 
+// Multicast forms: the same shared-memory offset and mbarrier offset in every CTA of `mask`
+// (thread-block cluster) receive the data and its complete_tx.
+MOE_DEV void tma_load_2d_mc(uint32_t dst, const void* tmap, int x, int y, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+MOE_DEV void tma_gather4_mc(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2, int y3, uint32_t bar,
+                            uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// thread-block clusters
+
+MOE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+MOE_DEV uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+MOE_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+MOE_DEV uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster (also orders this CTA's shared-memory writes, e.g.
+// mbarrier initialisation, before the other CTAs' later accesses).
+MOE_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05 (tensor memory and 5th-generation MMA), cta_group::1
 
@@ -149,6 +208,13 @@ MOE_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint
 // The mbarrier completes one arrival once every tcgen05 op issued so far by this thread is done.
 MOE_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// ... on the mbarrier at the same offset in every CTA of `mask`.
+MOE_DEV void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
                : "memory");
 }
 
@@ -223,38 +289,32 @@ MOE_DEV void e4m3x4_to_f16x2(uint32_t sc, uint32_t& a01, uint32_t& a23) {
       : "r"(sc));
 }
 
-// one f16x2 pair of exact products v = lut*scale -> BF16 pair of fp32(v * s2)
-MOE_DEV uint32_t scale_pair_to_bf16x2(uint32_t v, float s2) {
+// lut (f16 pair) * scale (one f16) -> two exact fp32 products (mixed-precision FMA with a -0
+// addend, so code 8 keeps its sign as -0), times
+// scale2 (packed fp32 multiply, the one rounding), -> BF16 pair (round to nearest even).
+MOE_DEV uint32_t dequant_pair(uint32_t lut2, uint32_t scale_h, float s2) {
   uint32_t out;
-  asm("{\n .reg .b16 lo, hi;\n .reg .f32 flo, fhi;\n .reg .b64 p, q, s;\n"
-      " mov.b32 {lo, hi}, %1;\n cvt.f32.f16 flo, lo;\n cvt.f32.f16 fhi, hi;\n"
-      " mov.b64 p, {flo, fhi};\n mov.b64 s, {%2, %2};\n mul.rn.f32x2 q, p, s;\n"
+  asm("{\n .reg .b16 lo, hi, a, unused;\n .reg .f32 flo, fhi;\n .reg .b64 p, q, s;\n"
+      " mov.b32 {lo, hi}, %1;\n mov.b32 {a, unused}, %2;\n"
+      " fma.rn.f32.f16 flo, lo, a, 0f80000000;\n fma.rn.f32.f16 fhi, hi, a, 0f80000000;\n"
+      " mov.b64 p, {flo, fhi};\n mov.b64 s, {%3, %3};\n mul.rn.f32x2 q, p, s;\n"
       " mov.b64 {flo, fhi}, q;\n cvt.rn.bf16x2.f32 %0, fhi, flo;\n}"
       : "=r"(out)
-      : "r"(v), "f"(s2));
+      : "r"(lut2), "r"(scale_h), "f"(s2));
   return out;
-}
-
-MOE_DEV uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 MOE_DEV void dequant64(const uint32_t (&w)[8], uint32_t sc, float s2, uint32_t (&out)[32]) {
   uint32_t a01, a23;
   e4m3x4_to_f16x2(sc, a01, a23);
-  uint32_t blk[4];
-  blk[0] = prmt(a01, a01, 0x1010u);  // (a0, a0)
-  blk[1] = prmt(a01, a01, 0x3232u);  // (a1, a1)
-  blk[2] = prmt(a23, a23, 0x1010u);
-  blk[3] = prmt(a23, a23, 0x3232u);
+  // block b's f16 scale in the low half of blk[b]
+  const uint32_t blk[4] = {a01, a01 >> 16, a23, a23 >> 16};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint32_t h[4];
     e2m1x8_to_f16x2(w[j], h);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) out[4 * j + q] = scale_pair_to_bf16x2(hmul2(h[q], blk[j >> 1]), s2);
+    for (int q = 0; q < 4; ++q) out[4 * j + q] = dequant_pair(h[q], blk[j >> 1], s2);
   }
 }
 

@@ -1,28 +1,33 @@
-// grouped_gemm.cu -- persistent grouped W4A16 GEMM for sm_103a (tcgen05 + TMA + TMEM).
+// grouped_gemm.cu -- persistent grouped W4A16 GEMM for sm_103a (tcgen05 + TMA + TMEM + clusters).
 //
 // One launch covers every expert ("Module forward_prefill_gemm", "What this replaces": one
 // launch for all experts, an expert_offsets prefix sum, the A gather through
 // sorted_token_ids inside the kernel).  For each expert e and sorted row p in
 // [off[e], off[e+1]):  C[p, n] = sum_k A[g(p), k] * Wdq_e[n, k].
 //
-// Work decomposition ("swap AB"): a tile is (expert e, 128 weight rows n0..n0+127, up to
-// BN_MAX of the expert's rows).  The 128 weight rows are the MMA's M operand and live in
-// TENSOR MEMORY: dequantisation warps turn the TMA-loaded NVFP4 bytes into BF16 and write them
-// with tcgen05.st straight into TMEM (no shared-memory round trip for A).  The expert's rows
-// (tokens) are the MMA's N operand (16..256 wide, padded to 16), gathered by TMA gather4 into
-// 128-byte-swizzled shared memory.  FP32 accumulators stay in TMEM until the epilogue.
+// Work decomposition ("swap AB"): a tile is (expert e, 128 weight rows, up to BN_MAX of the
+// expert's rows).  The 128 weight rows are the MMA's M operand and live in TENSOR MEMORY:
+// dequantisation warps turn the TMA-loaded NVFP4 bytes into BF16 and write them with tcgen05.st
+// straight into TMEM (no shared-memory round trip for A).  The expert's rows (tokens) are the
+// MMA's N operand (16..256 wide, padded to 16) in 128-byte-swizzled shared memory.  FP32
+// accumulators stay in TMEM until the epilogue.
 //
-// Tile order is (expert, n-block, token-block) with the token-block fastest, so the CTAs that
-// share one expert's weights run at the same time and the repeats hit L2: each expert's
-// packed weights and scales are read from HBM once per launch.  The static round-robin tile
-// walk is the persistent scheduler: it is driven by expert_offsets on the device, balances
-// skew by splitting heavy experts into many token blocks, and needs no host round trip.
+// Thread-block clusters of CL CTAs take CL consecutive 128-row weight blocks of the same
+// (expert, token block): they need the same activation rows, so each CTA fetches 1/CL of them
+// and multicasts them into all CL CTAs' shared memory (TMA gather4 for gathered rows, tiled
+// 16-row boxes for contiguous rows).  This divides the per-SM activation fetch by CL.
+//
+// Tile order is (expert, n-block group, token block) with the token block fastest, so the
+// clusters that share one expert's weights run at the same time and repeats hit L2: each
+// expert's packed weights and scales are read from HBM once per launch.  The static round-robin
+// walk over clusters is the persistent scheduler: it is driven by expert_offsets on the device,
+// balances skew by splitting heavy experts into many token blocks, and needs no host round trip.
 //
 // Warp roles (15 warps):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 -> shared staging -> 16-byte global stores
 //   4-11  dequantisation, two warpgroups taking alternate 64-k sub-stages
 //   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B])
-//   13    activation producer (TMA gather4, 4 rows per instruction)
+//   13    activation producer (this CTA's share of each stage, multicast to the cluster)
 //   14    MMA issuer (one thread) and TMEM owner
 // Every pipeline wait is bounded: on a timeout the CTA records MOE_DEVERR_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
@@ -46,12 +51,16 @@ constexpr int WARP_WP = 12, WARP_AP = 13, WARP_MMA = 14;
 constexpr int NUM_WARPS = 15;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int MAX_E = 1024;
+constexpr int ID_BOX_ROWS = 16;  // rows per tiled box when the A rows are contiguous
 
-template <int BN_MAX_, int NA_, int NW_>
+// BN_MAX: token-tile width (MMA N, at most 256); NA/NW: activation/weight ring depths;
+// ND: accumulator buffers in TMEM (2 lets the epilogue of one tile overlap the next tile's MMAs).
+template <int BN_MAX_, int NA_, int NW_, int ND_>
 struct Cfg {
   static constexpr int BN_MAX = BN_MAX_;
   static constexpr int NA = NA_;
   static constexpr int NW = NW_;
+  static constexpr int ND = ND_;
   static constexpr int ACT_STAGE = BN_MAX * 128;
   static constexpr int PK_STAGE = BM * 128;
   static constexpr int SC_STAGE = BM * 16;
@@ -63,33 +72,37 @@ struct Cfg {
   static constexpr int OFF_OFFS = OFF_EPI + 4 * EPI_WARP_BYTES;
   static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
   static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
-  // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full d_empty drain
-  static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 3;
+  // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full[ND] d_empty[ND] drain
+  static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 2 * ND + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
-  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256, "token tile");
+  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256 && ND * BN_MAX <= A_COL, "token tile / accumulator columns");
   static_assert(OFF_PK % 1024 == 0 && ACT_STAGE % 1024 == 0, "swizzled buffers need 1024-byte alignment");
+  static_assert(BYTES + 1024 <= 232448, "shared memory");
 };
 
 struct TileInfo {
   int e, nb, p0, cnt, bn;
 };
 
+// Group tile g of the cluster walk -> (expert, this CTA's n-block, token block).  Expert e owns
+// group tiles [s_tbase[e], s_tbase[e+1]); a group covers CL consecutive n-blocks.
 template <int BN_MAX>
-MOE_DEV TileInfo decode_tile(int t, const int* s_tbase, const int* s_offs, int E) {
-  int lo = 0, hi = E - 1;  // largest e in [0, E-1] with s_tbase[e] <= t
+MOE_DEV TileInfo decode_tile(int g, const int* s_tbase, const int* s_offs, int E, int CL, int rank) {
+  int lo = 0, hi = E - 1;  // largest e in [0, E-1] with s_tbase[e] <= g
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_tbase[mid] <= t) lo = mid; else hi = mid - 1;
+    if (s_tbase[mid] <= g) lo = mid; else hi = mid - 1;
   }
   TileInfo ti;
   ti.e = lo;
   const int m = s_offs[lo + 1] - s_offs[lo];
   const int ntt = (m + BN_MAX - 1) / BN_MAX;
-  const int local = t - s_tbase[lo];
-  ti.nb = local / ntt;
-  const int tt = local - ti.nb * ntt;
+  const int local = g - s_tbase[lo];
+  const int gb = local / ntt;
+  const int tt = local - gb * ntt;
+  ti.nb = gb * CL + rank;
   const int chunk = (((m + ntt - 1) / ntt) + 15) & ~15;
   ti.p0 = s_offs[lo] + tt * chunk;
   ti.cnt = min(chunk, m - tt * chunk);
@@ -120,9 +133,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto a_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + C::NA + s); };
   auto t_full = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + s); };
   auto t_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + NT + s); };
-  const uint32_t d_full = bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT);
-  const uint32_t d_empty = d_full + 8u;
-  const uint32_t drain_bar = d_full + 16u;
+  auto d_full = [&](int d) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + d); };
+  auto d_empty = [&](int d) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + C::ND + d); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + 2 * C::ND);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_bad = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
@@ -131,6 +144,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int E = args.E;
+  const int CL = (int)cluster_nctarank();
+  const int rank = (int)cluster_ctarank();
+  const int cid = (int)cluster_id_x();
+  const int ncl = (int)cluster_count_x();
+  const uint16_t mask = (uint16_t)((1u << CL) - 1u);
 
   if (tid == 0) {
     for (int s = 0; s < C::NW; ++s) {
@@ -139,14 +157,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int s = 0; s < C::NA; ++s) {
       mbar_init(a_full(s), 1);
-      mbar_init(a_empty(s), 1);
+      mbar_init(a_empty(s), CL);  // one commit from every CTA of the cluster that reads the stage
     }
     for (int s = 0; s < NT; ++s) {
       mbar_init(t_full(s), 4);
       mbar_init(t_empty(s), 1);
     }
-    mbar_init(d_full, 1);
-    mbar_init(d_empty, 4);
+    for (int d = 0; d < C::ND; ++d) {
+      mbar_init(d_full(d), 1);
+      mbar_init(d_empty(d), 4);
+    }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
     fence_barrier_init();
@@ -158,8 +178,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   for (int i = tid; i <= E; i += NUM_THREADS) s_offs[i] = args.offsets[i];
   __syncthreads();
 
-  // tile table: expert e owns tiles [s_tbase[e], s_tbase[e+1]); absent or empty experts own none
-  const int NB = (args.N + BM - 1) / BM;
+  // group-tile table: expert e owns [s_tbase[e], s_tbase[e+1]); absent or empty experts own none
+  const int NBG = (args.N + BM * CL - 1) / (BM * CL);  // n-block groups (the launch makes CL divide NB)
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
@@ -168,7 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int e = e0; e < e1; ++e) {
       const int m = s_offs[e + 1] - s_offs[e];
       if (m < 0) bad = true;
-      if (m > 0 && args.packed[e] != nullptr) sum += NB * ((m + C::BN_MAX - 1) / C::BN_MAX);
+      if (m > 0 && args.packed[e] != nullptr) sum += NBG * ((m + C::BN_MAX - 1) / C::BN_MAX);
     }
     if (lane == 0 && (s_offs[0] != 0 || s_offs[E] > args.R || s_offs[E] < 0)) bad = true;
     bad = __any_sync(0xffffffffu, bad);
@@ -182,14 +202,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int e = e0; e < e1; ++e) {
       s_tbase[e] = bad ? 0 : run;
       const int m = s_offs[e + 1] - s_offs[e];
-      if (m > 0 && args.packed[e] != nullptr) run += NB * ((m + C::BN_MAX - 1) / C::BN_MAX);
+      if (m > 0 && args.packed[e] != nullptr) run += NBG * ((m + C::BN_MAX - 1) / C::BN_MAX);
     }
     if (lane == 31) s_tbase[E] = bad ? 0 : incl;
     if (lane == 0) *s_bad = bad ? 1 : 0;
     if (bad && lane == 0 && blockIdx.x == 0) set_error(args.err, MOE_DEVERR_BAD_OFFSETS);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of every CTA initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int total = s_tbase[E];
@@ -214,19 +234,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
-      if (!warp_wait(d_full, it & 1, s_abort, args.err)) break;
+    for (int g = cid; g < total; g += ncl, ++it) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+      const int db = it % C::ND;
+      if (!warp_wait(d_full(db), (it / C::ND) & 1, s_abort, args.err)) break;
       tc_fence_after();
       const int n0 = ti.nb * BM + q * 32;
       for (int c0 = 0; c0 < ti.cnt; c0 += 32) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + D_COL + c0, v);
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + D_COL + db * C::BN_MAX + c0, v);
         tmem_wait_ld();
         if (c0 + 32 >= ti.cnt) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(d_empty);
+          if (lane == 0) mbar_arrive(d_empty(db));
         }
         __syncwarp();
         if (f32) {
@@ -260,8 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     int wi = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+    for (int g = cid; ok && g < total; g += ncl) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
       const float s2 = args.scale2[ti.e];
       for (int ks = 0; ks < KW; ++ks, ++wi) {
         const int s = wi % C::NW;
@@ -303,8 +324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int wi = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
+      for (int g = cid; ok && g < total; g += ncl) {
+        const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
         const CUtensorMap* mp = args.wmaps + 2 * ti.e;
         const CUtensorMap* ms = mp + 1;
         prefetch_tmap(mp);
@@ -322,22 +343,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == WARP_AP) {
     // ------------------------------------------------------------------ activation producer
+    // This CTA fetches the row groups grp with grp % CL == rank of each stage and multicasts them.
+    // Gathered rows: groups of 4 rows (TMA gather4); contiguous rows: 16-row tiled boxes.
+    constexpr int NH = (C::BN_MAX + 127) / 128;  // gather4 groups per lane per stage (CL = 1)
+    const bool gathered = args.gather != nullptr;
     int ai = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
-      const int ng = ti.bn >> 2;  // gather4 ops per stage
-      constexpr int NH = (C::BN_MAX + 127) / 128;  // gather4 ops per lane per stage
+    for (int g = cid; ok && g < total; g += ncl) {
+      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+      const int ng = gathered ? (ti.bn >> 2) : (ti.bn / ID_BOX_ROWS);  // row groups per stage
       int rows[NH * 4];
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const int g = lane + 32 * h;
+        const int grp = rank + CL * (lane + 32 * h);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          int p = ti.p0 + min(4 * g + r, ti.cnt - 1);
-          int src = args.gather ? args.gather[p] : p;
+          const int p = ti.p0 + min(4 * grp + r, ti.cnt - 1);
+          int src = gathered ? args.gather[p] : p;
           if ((unsigned)src >= (unsigned)args.a_rows) {
-            if (g < ng) set_error(args.err, MOE_DEVERR_BAD_GATHER);
+            if (gathered && grp < ng) set_error(args.err, MOE_DEVERR_BAD_GATHER);
             src = 0;
           }
           rows[4 * h + r] = src;
@@ -348,12 +372,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!warp_wait(a_empty(s), ((ai / C::NA) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(a_full(s), ti.bn * 128);
         __syncwarp();
+        const uint32_t dst0 = sbase + C::OFF_ACT + s * C::ACT_STAGE;
+        if (gathered) {
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int g = lane + 32 * h;
-          if (g < ng)
-            tma_gather4(sbase + C::OFF_ACT + s * C::ACT_STAGE + g * 512, &amap, kb * BKA, rows[4 * h],
-                        rows[4 * h + 1], rows[4 * h + 2], rows[4 * h + 3], a_full(s));
+          for (int h = 0; h < NH; ++h) {
+            const int grp = rank + CL * (lane + 32 * h);
+            if (grp < ng) {
+              if (CL > 1)
+                tma_gather4_mc(dst0 + grp * 512, &amap, kb * BKA, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
+                               rows[4 * h + 3], a_full(s), mask);
+              else
+                tma_gather4(dst0 + grp * 512, &amap, kb * BKA, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
+                            rows[4 * h + 3], a_full(s));
+            }
+          }
+        } else {
+          for (int grp = rank + CL * lane; grp < ng; grp += CL * 32) {
+            const int y = ti.p0 + grp * ID_BOX_ROWS;
+            if (CL > 1)
+              tma_load_2d_mc(dst0 + grp * ID_BOX_ROWS * 128, &amap, kb * BKA, y, a_full(s), mask);
+            else
+              tma_load_2d(dst0 + grp * ID_BOX_ROWS * 128, &amap, kb * BKA, y, a_full(s));
+          }
         }
       }
     }
@@ -364,11 +404,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int ai = 0, it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile<C::BN_MAX>(t, s_tbase, s_offs, E);
-        if (!mbar_wait(d_empty, (it & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+      for (int g = cid; ok && g < total; g += ncl, ++it) {
+        const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+        const int db = it % C::ND;
+        if (!mbar_wait(d_empty(db), ((it / C::ND) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t idesc = make_idesc_bf16(BM, ti.bn);
+        const uint32_t d_tmem = tmem_base + D_COL + db * C::BN_MAX;
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % C::NA;
           const int ts = ai % NT;
@@ -378,12 +420,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t bsm = sbase + C::OFF_ACT + s * C::ACT_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BKA / 16; ++kk)
-            mma_bf16_ts(tmem_base + D_COL, tmem_base + A_COL + ts * 32 + kk * 8, make_sdesc_sw128(bsm + kk * 32),
-                        idesc, (kb | kk) != 0);
-          mma_commit(a_empty(s));
+            mma_bf16_ts(d_tmem, tmem_base + A_COL + ts * 32 + kk * 8, make_sdesc_sw128(bsm + kk * 32), idesc,
+                        (kb | kk) != 0);
+          if (CL > 1) mma_commit_mc(a_empty(s), mask);  // the stage is free in every CTA once all read it
+          else mma_commit(a_empty(s));
           mma_commit(t_empty(ts));
         }
-        if (ok) mma_commit(d_full);
+        if (ok) mma_commit(d_full(db));
       }
       if (!ok) {
         mma_commit(drain_bar);
@@ -398,9 +441,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  cluster_sync_all();  // no CTA leaves while another may still multicast into it or signal it
 }
 
-using CfgLarge = Cfg<256, 3, 4>;
+using CfgS = Cfg<64, 10, 6, 2>;   // few rows per expert (HBM-bound): deep rings, small token tiles
+using CfgM = Cfg<128, 6, 5, 2>;   // ~100 rows per expert
+using CfgL = Cfg<256, 3, 4, 1>;   // hundreds of rows per expert (tensor-bound)
+
+template <class C>
+int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream_t stream) {
+  static int configured[64] = {0};
+  static int max_clusters[64][4] = {{0}};  // per device, per log2(CL)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  const int lg = CL == 8 ? 3 : CL == 4 ? 2 : CL == 2 ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev][lg] == 0) {
+    cfg.gridDim = dim3(CL * device_sm_count());
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+    max_clusters[dev][lg] = n;
+  }
+  const long long nbg = (args.N + BM * CL - 1) / (BM * CL);
+  const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
+  const int ncl = (int)std::max<long long>(1, std::min<long long>(max_clusters[dev][lg], max_groups));
+  cfg.gridDim = dim3(ncl * CL);
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<C>, amap, args) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// cluster width: the largest of 8, 4, 2 that divides the number of 128-row weight blocks
+int cluster_width(int N) {
+  const int nb = (N + BM - 1) / BM;
+  for (int c : {8, 4, 2})
+    if (nb % c == 0) return c;
+  return 1;
+}
 
 }  // namespace gg
 
@@ -408,33 +500,23 @@ using CfgLarge = Cfg<256, 3, 4>;
 // host side
 
 int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda, cudaStream_t stream) {
-  using C = gg::CfgLarge;
+  const bool gathered = args.gather != nullptr;
   CUtensorMap amap;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)a_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
-    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t box[2] = {64, gathered ? 1u : (cuuint32_t)gg::ID_BOX_ROWS};
     const cuuint32_t estr[2] = {1, 1};
     int rc = encode_tmap(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box, estr,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MOE_OK) return rc;
   }
-  static int configured_device = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (configured_device != dev) {
-    if (cudaFuncSetAttribute(gg::grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    configured_device = dev;
-  }
-  const int nsm = device_sm_count();
-  if (nsm <= 0) return MOE_ERR_CUDA;
-  const long long nb = (args.N + gg::BM - 1) / gg::BM;
-  const long long max_tiles = nb * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
-  const int grid = (int)std::max<long long>(1, std::min<long long>(nsm, max_tiles));
-  gg::grouped_gemm_kernel<C><<<grid, gg::NUM_THREADS, C::SMEM_ALLOC, stream>>>(amap, args);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int CL = gg::cluster_width(args.N);
+  // token-tile width from the mean rows per expert (the distribution itself is on the device)
+  const double mean_rows = (double)args.R / args.E;
+  if (mean_rows <= 48.0) return gg::launch_cfg<gg::CfgS>(amap, args, CL, stream);
+  if (mean_rows <= 160.0) return gg::launch_cfg<gg::CfgM>(amap, args, CL, stream);
+  return gg::launch_cfg<gg::CfgL>(amap, args, CL, stream);
 }
 
 }  // namespace moe

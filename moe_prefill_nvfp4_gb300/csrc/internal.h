@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe_prefill.h"
+#include "moe_prefill.h"
 
 namespace moe {
 

@@ -182,81 +182,145 @@ int route_topk_launch(const float* logits, const float* bias, int T, int E, int 
 }
 
 // ------------------------------------------------------------------------------------------------
-// stable expert sort.  The R slots are cut into S segments; warp (b, seg) handles bucket b
-// (expert b, or the tail b = E for -1 / invalid ids) in one segment:
-//   count:   cnt[b*S + seg] = number of slots of the segment in bucket b  (ballot + popc)
-//   scatter: base = sum of cnt before (b, seg) in bucket-major order = the sorted position of the
-//            bucket's first slot of the segment; the ballot prefix within each 32-slot chunk
-//            keeps flat slot order, so the sort is stable.
+// stable expert sort.  The R slots are cut into segments of SORT_SEG; bucket b is expert b, or
+// the tail b = E for -1 / invalid ids.
+//   hist:    one block per segment counts its slots per bucket in shared memory -> cnt[b*S + seg]
+//   scatter: one block per segment; the sorted position of a slot is
+//              (slots of all buckets < b) + (slots of bucket b in earlier segments)
+//              + (slots of bucket b earlier in this segment),
+//            the last term from __match_any_sync ranks inside 32-slot chunks plus per-warp running
+//            counts, which keeps flat slot order (a stable sort).  Block 0 writes expert_offsets.
 
-constexpr int SORT_WARPS = 8;
+constexpr int SORT_SEG = 2048;
+constexpr int SORT_THREADS = 256;
+constexpr int SORT_WARPS = SORT_THREADS / 32;
+constexpr int SORT_PER_WARP = SORT_SEG / SORT_WARPS;
 
 int sort_segments(int R, int E) {
-  const int by_size = (R + 2047) / 2048;
-  const int by_prefix = std::max(1, 2048 / (E + 1));
-  return std::max(1, std::min(64, std::min(by_size, by_prefix)));
+  (void)E;
+  return std::max(1, (R + SORT_SEG - 1) / SORT_SEG);
 }
 
 size_t sort_scratch_bytes(int R, int E) { return (size_t)(E + 1) * sort_segments(R, E) * sizeof(int32_t); }
 
-MOE_DEV bool in_bucket(int id, int b, int E) { return b < E ? id == b : (id < 0 || id >= E); }
+MOE_DEV int bucket_of(int id, int E) { return (id >= 0 && id < E) ? id : E; }
 
-__global__ void __launch_bounds__(SORT_WARPS * 32)
-    sort_count_kernel(const int32_t* __restrict__ ids, int R, int E, int S, int32_t* __restrict__ cnt, int* err) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = blockIdx.x * SORT_WARPS + warp;
-  if (gid >= (E + 1) * S) return;
-  const int b = gid / S, seg = gid - b * S;
-  const int L = (R + S - 1) / S;
-  const int lo = seg * L, hi = min(R, lo + L);
-  int c = 0;
+__global__ void __launch_bounds__(SORT_THREADS)
+    sort_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int S, int32_t* __restrict__ cnt, int* err) {
+  extern __shared__ int s_hist[];
+  const int seg = blockIdx.x;
+  for (int b = threadIdx.x; b <= E; b += SORT_THREADS) s_hist[b] = 0;
+  __syncthreads();
+  const int lo = seg * SORT_SEG, hi = min(R, lo + SORT_SEG);
   bool bad = false;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const int id = i < hi ? ids[i] : -2;
-    if (b == E && i < hi && (id < -1 || id >= E)) bad = true;
-    c += __popc(__ballot_sync(0xffffffffu, i < hi && in_bucket(id, b, E)));
+  for (int i = lo + threadIdx.x; i < hi; i += SORT_THREADS) {
+    const int id = ids[i];
+    if (id < -1 || id >= E) bad = true;
+    atomicAdd(&s_hist[bucket_of(id, E)], 1);
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
-  if (lane == 0) cnt[gid] = c;
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
+  for (int b = threadIdx.x; b <= E; b += SORT_THREADS) cnt[b * S + seg] = s_hist[b];
 }
 
-__global__ void __launch_bounds__(SORT_WARPS * 32)
+__global__ void __launch_bounds__(SORT_THREADS)
     sort_scatter_kernel(const int32_t* __restrict__ ids, int R, int k, int E, int S, const int32_t* __restrict__ cnt,
                         int32_t* __restrict__ sorted_token_ids, int32_t* __restrict__ sorted_expert_ids,
                         int32_t* __restrict__ expert_offsets, int32_t* __restrict__ token_to_perm) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = blockIdx.x * SORT_WARPS + warp;
-  if (gid >= (E + 1) * S) return;
-  const int b = gid / S, seg = gid - b * S;
-  int base = 0;
-  for (int i = lane; i < gid; i += 32) base += cnt[i];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) base += __shfl_xor_sync(0xffffffffu, base, o);
-  if (seg == 0 && lane == 0) expert_offsets[b] = base;  // b == E: number of valid slots
-  const int L = (R + S - 1) / S;
-  const int lo = seg * L, hi = min(R, lo + L);
-  const uint32_t lt = (1u << lane) - 1u;
-  int run = base;
-  for (int start = lo; start < hi; start += 32) {
-    const int i = start + lane;
-    const int id = i < hi ? ids[i] : -2;
-    const bool m = i < hi && in_bucket(id, b, E);
-    const uint32_t bal = __ballot_sync(0xffffffffu, m);
-    if (m) {
-      const int p = run + __popc(bal & lt);
-      sorted_token_ids[p] = i / k;
-      sorted_expert_ids[p] = b < E ? b : -1;
-      token_to_perm[i] = b < E ? p : -1;
-    }
-    run += __popc(bal);
+  extern __shared__ int s_mem[];
+  const int NB = E + 1;
+  int* s_base = s_mem;                                              // [NB]
+  int16_t* s_wcnt = reinterpret_cast<int16_t*>(s_base + NB);        // [SORT_WARPS][NB]
+  int16_t* s_lpos = s_wcnt + SORT_WARPS * NB;                       // [SORT_SEG]
+  int16_t* s_bkt = s_lpos + SORT_SEG;                               // [SORT_SEG]
+  const int seg = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // (1) total slots per bucket over all segments
+  for (int b = tid; b < NB; b += SORT_THREADS) {
+    int tot = 0;
+    for (int s = 0; s < S; ++s) tot += cnt[b * S + s];
+    s_base[b] = tot;
   }
+  __syncthreads();
+  // exclusive prefix of the totals over buckets (warp 0: each lane a contiguous run)
+  if (warp == 0) {
+    const int per = (NB + 31) / 32;
+    const int b0 = min(NB, lane * per), b1 = min(NB, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += s_base[b];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int b = b0; b < b1; ++b) {
+      const int t = s_base[b];
+      s_base[b] = run;
+      if (seg == 0) expert_offsets[b] = run;  // b == E: number of valid slots
+      run += t;
+    }
+  }
+  __syncthreads();
+  // ... plus this bucket's slots in the earlier segments
+  for (int b = tid; b < NB; b += SORT_THREADS) {
+    int own = 0;
+    for (int s = 0; s < seg; ++s) own += cnt[b * S + s];
+    s_base[b] += own;
+  }
+  for (int i = tid; i < SORT_WARPS * NB; i += SORT_THREADS) s_wcnt[i] = 0;
+  __syncthreads();
+
+  // (2) stable ranks inside the segment
+  const int lo = seg * SORT_SEG, hi = min(R, lo + SORT_SEG);
+  const uint32_t lt = (1u << lane) - 1u;
+  int16_t* wc = s_wcnt + warp * NB;
+  for (int c = 0; c < SORT_PER_WARP; c += 32) {
+    const int li = warp * SORT_PER_WARP + c + lane;  // slot index inside the segment
+    const int i = lo + li;
+    const int b = i < hi ? bucket_of(ids[i], E) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    int local = 0;
+    if (b >= 0) local = wc[b] + __popc(peers & lt);
+    __syncwarp();
+    if (b >= 0 && (__ffs(peers) - 1) == lane) wc[b] = (int16_t)(wc[b] + __popc(peers));
+    __syncwarp();
+    s_lpos[li] = (int16_t)local;
+    s_bkt[li] = (int16_t)b;
+  }
+  __syncthreads();
+  // (3) per bucket, exclusive prefix over the warps
+  for (int b = tid; b < NB; b += SORT_THREADS) {
+    int run = 0;
+    for (int w = 0; w < SORT_WARPS; ++w) {
+      const int t = s_wcnt[w * NB + b];
+      s_wcnt[w * NB + b] = (int16_t)run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  // (4) write
+  for (int li = tid; li < SORT_SEG; li += SORT_THREADS) {
+    const int i = lo + li;
+    if (i >= hi) break;
+    const int b = s_bkt[li];
+    const int w = li / SORT_PER_WARP;
+    const int p = s_base[b] + s_wcnt[w * NB + b] + s_lpos[li];
+    sorted_token_ids[p] = i / k;
+    sorted_expert_ids[p] = b < E ? b : -1;
+    token_to_perm[i] = b < E ? p : -1;
+  }
+}
+
+static size_t scatter_smem(int E) {
+  const int NB = E + 1;
+  return (size_t)NB * 4 + (size_t)SORT_WARPS * NB * 2 + (size_t)SORT_SEG * 2 * 2;
 }
 
 int sort_count_launch(const int32_t* ids, int R, int E, int32_t* cnt, int* err, cudaStream_t st) {
   const int S = sort_segments(R, E);
-  const int warps = (E + 1) * S;
-  sort_count_kernel<<<(warps + SORT_WARPS - 1) / SORT_WARPS, SORT_WARPS * 32, 0, st>>>(ids, R, E, S, cnt, err);
+  sort_hist_kernel<<<S, SORT_THREADS, (E + 1) * sizeof(int), st>>>(ids, R, E, S, cnt, err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -264,9 +328,8 @@ int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* 
                         int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
                         cudaStream_t st) {
   const int S = sort_segments(R, E);
-  const int warps = (E + 1) * S;
-  sort_scatter_kernel<<<(warps + SORT_WARPS - 1) / SORT_WARPS, SORT_WARPS * 32, 0, st>>>(
-      ids, R, k, E, S, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm);
+  sort_scatter_kernel<<<S, SORT_THREADS, scatter_smem(E), st>>>(ids, R, k, E, S, cnt, sorted_token_ids,
+                                                               sorted_expert_ids, expert_offsets, token_to_perm);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -1,9 +1,18 @@
 """GPU parity of the whole routed-MoE prefill path (moe_prefill_forward) against the oracle.
 
 Routing and the sort are compared bit-exactly on shared logits (the GPU's router logits are
-fed to the oracle's top-k, so a different summation order cannot flip a near tie); every
-float stage (wts, G, act, Y, out) within the tolerances.  Full-size workloads are checked on
-sampled tokens, which the oracle computes one token at a time.
+fed to the oracle's top-k, so a different summation order cannot flip a near tie).
+
+Float stages (wts, G, act, Y, out):
+* against the BF16-rounding oracle, stage by stage: each stage's GPU output against the oracle
+  applied to the same BF16 input the GPU stage consumed (G from x, act from the GPU's G, Y from
+  the GPU's act, out from the GPU's Y), within 4e-3 of max|ref|;
+* against the exact-FP32 oracle, as one independent chain from x to out, within 1e-2.
+A whole independent BF16 chain is not held to 4e-3: when FP32 summation order flips a BF16
+rounding of G (about 0.2% of elements), the flip propagates through act and Y, and with
+concentrated routing weights it alone can move out by ~2e-3 of max|out| on top of out's own
+rounding (up to 2^-8).  Its value is recorded in the assertion message of the exact check.
+Full-size workloads are checked on sampled tokens, which the oracle computes one at a time.
 """
 
 import numpy as np
@@ -27,26 +36,44 @@ def _no_device_error():
     assert moe.moe_get_device_error() == 0
 
 
-def _check_full(case, variants=("bf16", "exact")):
+def _stagewise(case, st, R):
+    """Oracle of each float stage on the GPU's own BF16 stage inputs (BF16-rounding variant)."""
+    I = case.I
+    off = st["expert_offsets"]
+    dn = lambda e: (None if case.down.packed[e] is None else
+                    O.dequant_nvfp4(case.down.packed[e], case.down.scales[e], case.down.scale2[e], "bf16"))
+    act = O.swiglu_clamp(st["G"][:R, :I], st["G"][:R, I:], case.swiglu_limit)
+    Y = O.grouped_gemm(st["act"][:R], off, dn)
+    out = O.combine_indexed(st["Y"], st["token_to_perm"], st["wts"].astype(np.float64))
+    return act, Y, out
+
+
+def _check_full(case):
     db = DeviceBlock(case)
     db.forward()
     torch.cuda.synchronize()
     st = db.stages()
     db.close()
-    for v in variants:
-        ref = O.prefill_forward(case, v, logits=st["logits"])
-        if case.router_w is not None and v == "bf16":
-            assert nerr(st["logits"], O.router_logits(case.x, case.router_w)) < 1e-5
-        for key in ("ids", "sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm"):
-            np.testing.assert_array_equal(st[key], ref[key], err_msg=key)
-        np.testing.assert_allclose(st["wts"], ref["wts"], rtol=2e-6, atol=1e-7)
-        R = int(ref["expert_offsets"][-1])
-        tol = TOL_BF16 if v == "bf16" else TOL_EXACT
-        for key in ("G", "act", "Y"):
-            e = nerr(st[key][:R], ref[key + "64"][:R])
-            assert e < tol, (v, key, e)
-        e = nerr(st["out"], ref["out64"])
-        assert e < tol, (v, "out", e)
+    # without a router the forward routes on the caller's logits and leaves the workspace's
+    # logits buffer unwritten
+    shared_logits = st["logits"] if case.router_w is not None else case.logits
+    if case.router_w is not None:
+        assert nerr(st["logits"], O.router_logits(case.x, case.router_w)) < 1e-5
+    chains = {v: O.prefill_forward(case, v, logits=shared_logits) for v in ("bf16", "exact")}
+    ref = chains["bf16"]
+    for key in ("ids", "sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm"):
+        np.testing.assert_array_equal(st[key], ref[key], err_msg=key)
+    np.testing.assert_allclose(st["wts"], ref["wts"], rtol=2e-6, atol=1e-7)
+    R = int(ref["expert_offsets"][-1])
+    act, Y, out = _stagewise(case, st, R)
+    errs = {"G": nerr(st["G"][:R], ref["G64"][:R]), "act": nerr(st["act"][:R], act), "Y": nerr(st["Y"][:R], Y),
+            "out": nerr(st["out"], out)}
+    assert all(e < TOL_BF16 for e in errs.values()), ("bf16 stage-wise", errs)
+    ex = chains["exact"]
+    chain = {k: nerr(st[k][:R] if k != "out" else st[k], ex[k + "64"][:R] if k != "out" else ex["out64"])
+             for k in ("G", "act", "Y", "out")}
+    chain_bf16 = nerr(st["out"], ref["out64"])
+    assert all(e < TOL_EXACT for e in chain.values()), ("exact chain", chain, "bf16 chain out", chain_bf16)
 
 
 def test_small_ragged_block():
@@ -70,14 +97,22 @@ def test_c1_full_chunk():
 
 
 def _check_sampled(case, tokens, variants=("bf16",)):
+    """Sampled tokens at full size.  The sample always contains the tokens holding the largest
+    |out|, |G| and |Y| of the GPU tensors, so the denominator max|ref| over the sampled rows is
+    the full tensor's ||ref||_inf, as in the tolerance's definition; the numerator is the max
+    over the sampled rows."""
     db = DeviceBlock(case)
     db.forward()
     torch.cuda.synchronize()
     T, k, E, H, I = case.T, case.k, case.E, case.H, case.I
+    R = T * k
     ids = db.ws_view("ids", torch.int32, (T, k)).cpu().numpy()
     wts = db.ws_view("wts", torch.float32, (T, k)).cpu().numpy()
     t2p = db.ws_view("token_to_perm", torch.int32, (T, k)).cpu().numpy()
     off = db.ws_view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy()
+    sti = db.ws_view("sorted_token_ids", torch.int32, (R,))
+    Gd = db.ws_view("G", torch.bfloat16, (R, 2 * I))
+    Yd = db.ws_view("Y", torch.bfloat16, (R, H))
     # routing and the sort at full size, bit-exact
     rid, rw = O.route_topk(case.logits, k)
     np.testing.assert_array_equal(ids, rid)
@@ -85,18 +120,32 @@ def _check_sampled(case, tokens, variants=("bf16",)):
     srt = O.sort_by_expert(rid, E)
     np.testing.assert_array_equal(off, srt["expert_offsets"])
     np.testing.assert_array_equal(t2p, srt["token_to_perm"])
+    np.testing.assert_array_equal(sti.cpu().numpy(), srt["sorted_token_ids"])
+    nvalid = int(off[E])
+    extra = [int(db.out.abs().amax(1).argmax()),
+             int(sti[int(Gd[:nvalid].abs().amax(1).argmax())]),
+             int(sti[int(Yd[:nvalid].abs().amax(1).argmax())])]
+    tokens = sorted(set(list(tokens) + extra))
     out = bf16_host(db.out[tokens])
-    rows = t2p[tokens].reshape(-1)
-    G = bf16_host(db.ws_view("G", torch.bfloat16, (T * k, 2 * I))[torch.from_numpy(rows).long().cuda()])
-    Y = bf16_host(db.ws_view("Y", torch.bfloat16, (T * k, H))[torch.from_numpy(rows).long().cuda()])
+    rows = torch.from_numpy(t2p[tokens].reshape(-1)).long().cuda()
+    G = bf16_host(Gd[rows])
+    Y = bf16_host(Yd[rows])
+    A = bf16_host(db.ws_view("act", torch.bfloat16, (R, I))[rows])
+    # bf16 variant, stage by stage on the GPU's own stage inputs
+    dq = {}
+    ref = O.token_forward(case, tokens, rid, rw, "bf16", dq)
+    eg = nerr(G, ref["G64"].reshape(-1, 2 * I))
+    ea = nerr(A, O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))
+    ys = np.stack([A[r] @ dq["dn"](int(e)).astype(np.float64).T for r, e in enumerate(rid[tokens].reshape(-1))])
+    ey = nerr(Y, ys)
+    perm = np.arange(len(tokens) * k, dtype=np.int32).reshape(len(tokens), k)
+    eo = nerr(out, O.combine_indexed(Y, perm, rw[tokens]))
+    assert max(eg, ea, ey, eo) < TOL_BF16, ("bf16 stage-wise", tokens, eg, ea, ey, eo)
+    if "exact" in variants:
+        ex = O.token_forward(case, tokens, rid, rw, "exact")
+        chain = (nerr(G, ex["G64"].reshape(-1, 2 * I)), nerr(Y, ex["Y64"].reshape(-1, H)), nerr(out, ex["out64"]))
+        assert max(chain) < TOL_EXACT, ("exact chain", tokens, chain, "bf16 chain out", nerr(out, ref["out64"]))
     db.close()
-    for v in variants:
-        ref = O.token_forward(case, tokens, rid, rw, v)
-        tol = TOL_BF16 if v == "bf16" else TOL_EXACT
-        assert nerr(G, ref["G64"].reshape(-1, 2 * I)) < tol, (v, "G")
-        assert nerr(Y, ref["Y64"].reshape(-1, H)) < tol, (v, "Y")
-        e = nerr(out, ref["out64"])
-        assert e < tol, (v, "out", e)
 
 
 def test_c2_glm_chunk_sampled():
@@ -106,7 +155,7 @@ def test_c2_glm_chunk_sampled():
 
 def test_c3_zipf_skew_sampled():
     c = S.workload("c3")
-    _check_sampled(c, [5, 8191])
+    _check_sampled(c, [5, 8191], variants=("bf16", "exact"))
 
 
 @pytest.mark.parametrize("T", [8, 16384])

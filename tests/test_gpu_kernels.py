@@ -244,3 +244,14 @@ def test_gemm_deterministic_and_bad_offsets():
     assert (out == 7.0).all()  # nothing written
     proj.close()
     proj2.close()
+
+
+@pytest.mark.parametrize("T,E,k", [(40, 16, 8), (300, 24, 8), (600, 4, 2)], ids=["64-row-tiles", "128-row-tiles",
+                                                                            "256-row-tiles"])
+def test_gemm_each_tile_config(T, E, k):
+    """Mean rows per expert ~20, ~100 and ~300 select the three token-tile widths."""
+    c = S.make_gemm_case(T=T, E=E, k=k, N=384, K=1024, seed=23 + T)
+    C, srt, proj = _gemm_case(c)
+    ref = _oracle_gemm(c, srt, "bf16")
+    assert nerr(C.cpu().numpy().astype(np.float64), ref) < 2e-6
+    proj.close()

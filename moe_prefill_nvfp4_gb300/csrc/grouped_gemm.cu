@@ -23,12 +23,16 @@
 // walk over clusters is the persistent scheduler: it is driven by expert_offsets on the device,
 // balances skew by splitting heavy experts into many token blocks, and needs no host round trip.
 //
-// Warp roles (15 warps):
+// A CTA owns NBLK (1 or 2) adjacent 128-row weight blocks that share the activation tile; each
+// block has its own accumulator and its own MMA-issuing warp (one thread issues an MMA only every
+// ~60-120 cycles, so small token tiles need more than one issuer per SM).
+//
+// Warp roles (16 warps):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 -> shared staging -> 16-byte global stores
 //   4-11  dequantisation, two warpgroups taking alternate 64-k sub-stages
-//   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B])
+//   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B] per block)
 //   13    activation producer (this CTA's share of each stage, multicast to the cluster)
-//   14    MMA issuer (one thread) and TMEM owner
+//   14-15 MMA issuers (one thread each, block 0 / block 1); warp 14 owns TMEM
 // Every pipeline wait is bounded: on a timeout the CTA records MOE_DEVERR_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 
@@ -43,27 +47,31 @@ namespace gg {
 constexpr int BM = 128;      // weight rows per tile = MMA M = TMEM lanes
 constexpr int BKW = 256;     // k per weight stage (128 packed bytes per row)
 constexpr int BKA = 64;      // k per activation stage and per TMEM A stage
-constexpr int NT = 8;        // TMEM A stages (32 columns each)
 constexpr int TMEM_COLS = 512;
-constexpr int D_COL = 0;     // accumulator columns [0, 256)
-constexpr int A_COL = 256;   // A stages at [256, 512)
+constexpr int D_COL = 0;     // accumulators first, then the A stages
 constexpr int WARP_WP = 12, WARP_AP = 13, WARP_MMA = 14;
-constexpr int NUM_WARPS = 15;
+constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int MAX_E = 1024;
 constexpr int ID_BOX_ROWS = 16;  // rows per tiled box when the A rows are contiguous
 
 // BN_MAX: token-tile width (MMA N, at most 256); NA/NW: activation/weight ring depths;
-// ND: accumulator buffers in TMEM (2 lets the epilogue of one tile overlap the next tile's MMAs).
-template <int BN_MAX_, int NA_, int NW_, int ND_>
+// ND: accumulator buffers per block (2 lets the epilogue of one tile overlap the next tile's
+// MMAs); NBLK: 128-row weight blocks per CTA.  TMEM: ND*NBLK*BN_MAX accumulator columns, the
+// rest holds NT A stages of 32*NBLK columns (64 k of every block).
+template <int BN_MAX_, int NA_, int NW_, int ND_, int NBLK_>
 struct Cfg {
   static constexpr int BN_MAX = BN_MAX_;
   static constexpr int NA = NA_;
   static constexpr int NW = NW_;
   static constexpr int ND = ND_;
+  static constexpr int NBLK = NBLK_;
+  static constexpr int ROWS = BM * NBLK;
+  static constexpr int A_COL = ND * NBLK * BN_MAX;
+  static constexpr int NT = (TMEM_COLS - A_COL) / (32 * NBLK);
   static constexpr int ACT_STAGE = BN_MAX * 128;
-  static constexpr int PK_STAGE = BM * 128;
-  static constexpr int SC_STAGE = BM * 16;
+  static constexpr int PK_STAGE = ROWS * 128;
+  static constexpr int SC_STAGE = ROWS * 16;
   static constexpr int EPI_WARP_BYTES = 32 * 32 * 4;
   static constexpr int OFF_ACT = 0;
   static constexpr int OFF_PK = OFF_ACT + NA * ACT_STAGE;
@@ -72,12 +80,13 @@ struct Cfg {
   static constexpr int OFF_OFFS = OFF_EPI + 4 * EPI_WARP_BYTES;
   static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
   static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
-  // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full[ND] d_empty[ND] drain
-  static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 2 * ND + 1;
+  // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full[ND] d_empty[ND]
+  // drain[NBLK]
+  static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 2 * ND + NBLK;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
-  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256 && ND * BN_MAX <= A_COL, "token tile / accumulator columns");
+  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256 && A_COL % 32 == 0 && NT >= 2, "token tile / TMEM columns");
   static_assert(OFF_PK % 1024 == 0 && ACT_STAGE % 1024 == 0, "swizzled buffers need 1024-byte alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
 };
@@ -86,9 +95,9 @@ struct TileInfo {
   int e, nb, p0, cnt, bn;
 };
 
-// Group tile g of the cluster walk -> (expert, this CTA's n-block, token block).  Expert e owns
-// group tiles [s_tbase[e], s_tbase[e+1]); a group covers CL consecutive n-blocks.
-template <int BN_MAX>
+// Group tile g of the cluster walk -> (expert, this CTA's first n-block, token block).  Expert e
+// owns group tiles [s_tbase[e], s_tbase[e+1]); a group covers CL * NBLK consecutive n-blocks.
+template <int BN_MAX, int NBLK>
 MOE_DEV TileInfo decode_tile(int g, const int* s_tbase, const int* s_offs, int E, int CL, int rank) {
   int lo = 0, hi = E - 1;  // largest e in [0, E-1] with s_tbase[e] <= g
   while (lo < hi) {
@@ -102,7 +111,7 @@ MOE_DEV TileInfo decode_tile(int g, const int* s_tbase, const int* s_offs, int E
   const int local = g - s_tbase[lo];
   const int gb = local / ntt;
   const int tt = local - gb * ntt;
-  ti.nb = gb * CL + rank;
+  ti.nb = (gb * CL + rank) * NBLK;
   const int chunk = (((m + ntt - 1) / ntt) + 15) & ~15;
   ti.p0 = s_offs[lo] + tt * chunk;
   ti.cnt = min(chunk, m - tt * chunk);
@@ -131,11 +140,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto w_empty = [&](int s) { return bar0 + 8u * (C::NW + s); };
   auto a_full = [&](int s) { return bar0 + 8u * (2 * C::NW + s); };
   auto a_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + C::NA + s); };
+  constexpr int NT = C::NT;
   auto t_full = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + s); };
   auto t_empty = [&](int s) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + NT + s); };
   auto d_full = [&](int d) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + d); };
   auto d_empty = [&](int d) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + C::ND + d); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + 2 * C::ND);
+  auto drain_bar = [&](int b) { return bar0 + 8u * (2 * C::NW + 2 * C::NA + 2 * NT + 2 * C::ND + b); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_bad = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
@@ -157,17 +167,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int s = 0; s < C::NA; ++s) {
       mbar_init(a_full(s), 1);
-      mbar_init(a_empty(s), CL);  // one commit from every CTA of the cluster that reads the stage
+      mbar_init(a_empty(s), CL * C::NBLK);  // one commit from every MMA warp of the cluster
     }
     for (int s = 0; s < NT; ++s) {
       mbar_init(t_full(s), 4);
-      mbar_init(t_empty(s), 1);
+      mbar_init(t_empty(s), C::NBLK);
     }
     for (int d = 0; d < C::ND; ++d) {
-      mbar_init(d_full(d), 1);
+      mbar_init(d_full(d), C::NBLK);
       mbar_init(d_empty(d), 4);
     }
-    mbar_init(drain_bar, 1);
+    for (int b = 0; b < C::NBLK; ++b) mbar_init(drain_bar(b), 1);
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -179,7 +189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
 
   // group-tile table: expert e owns [s_tbase[e], s_tbase[e+1]); absent or empty experts own none
-  const int NBG = (args.N + BM * CL - 1) / (BM * CL);  // n-block groups (the launch makes CL divide NB)
+  const int NBG = (args.N + BM * CL * C::NBLK - 1) / (BM * CL * C::NBLK);  // n-block groups (CL*NBLK divides NB)
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
@@ -235,40 +245,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     int it = 0;
     for (int g = cid; g < total; g += ncl, ++it) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+      const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
       const int db = it % C::ND;
       if (!warp_wait(d_full(db), (it / C::ND) & 1, s_abort, args.err)) break;
       tc_fence_after();
-      const int n0 = ti.nb * BM + q * 32;
-      for (int c0 = 0; c0 < ti.cnt; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + D_COL + db * C::BN_MAX + c0, v);
-        tmem_wait_ld();
-        if (c0 + 32 >= ti.cnt) {
-          tc_fence_before();
+      for (int b = 0; b < C::NBLK; ++b) {
+        const int n0 = (ti.nb + b) * BM + q * 32;
+        const uint32_t dcol = D_COL + (db * C::NBLK + b) * C::BN_MAX;
+        for (int c0 = 0; c0 < ti.cnt; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + dcol + c0, v);
+          tmem_wait_ld();
+          if (b == C::NBLK - 1 && c0 + 32 >= ti.cnt) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(d_empty(db));
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(d_empty(db));
-        }
-        __syncwarp();
-        if (f32) {
-          float* s = reinterpret_cast<float*>(stg);
+          if (f32) {
+            float* s = reinterpret_cast<float*>(stg);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __uint_as_float(v[j]);
-        } else {
-          __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
+            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __uint_as_float(v[j]);
+          } else {
+            __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
-        }
-        __syncwarp();
-        const int rows = min(32, ti.cnt - c0);
-        const int cpr = 32 * esz / 16;  // 16-byte chunks per staged row (4 bf16, 8 f32)
-        for (int c = lane; c < 32 * cpr; c += 32) {
-          const int r = c / cpr, cc = c - r * cpr;
-          const int n = n0 + cc * (16 / esz);
-          if (r < rows && n < args.N) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 * esz + cc * 16);
-            uint8_t* dst = reinterpret_cast<uint8_t*>(args.C) + ((size_t)(ti.p0 + c0 + r) * args.ldc + n) * esz;
-            *reinterpret_cast<uint4*>(dst) = val;
+            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          }
+          __syncwarp();
+          const int rows = min(32, ti.cnt - c0);
+          const int cpr = 32 * esz / 16;  // 16-byte chunks per staged row (4 bf16, 8 f32)
+          for (int c = lane; c < 32 * cpr; c += 32) {
+            const int r = c / cpr, cc = c - r * cpr;
+            const int n = n0 + cc * (16 / esz);
+            if (r < rows && n < args.N) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 * esz + cc * 16);
+              uint8_t* dst = reinterpret_cast<uint8_t*>(args.C) + ((size_t)(ti.p0 + c0 + r) * args.ldc + n) * esz;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
           }
         }
       }
@@ -282,19 +295,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int wi = 0;
     bool ok = true;
     for (int g = cid; ok && g < total; g += ncl) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+      const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
       const float s2 = args.scale2[ti.e];
       for (int ks = 0; ks < KW; ++ks, ++wi) {
         const int s = wi % C::NW;
         if (!warp_wait(w_full(s), (wi / C::NW) & 1, s_abort, args.err)) { ok = false; break; }
-        const uint8_t* pk = smem + C::OFF_PK + s * C::PK_STAGE + row * 128;
-        const uint4 scv = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + s * C::SC_STAGE + row * 16);
-        uint4 chunk[4];
+        uint4 chunk[C::NBLK][4];
+        uint4 scv[C::NBLK];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int sub = wg + 2 * h;
-          chunk[2 * h] = *reinterpret_cast<const uint4*>(pk + (((2 * sub) ^ (row & 7)) << 4));
-          chunk[2 * h + 1] = *reinterpret_cast<const uint4*>(pk + (((2 * sub + 1) ^ (row & 7)) << 4));
+        for (int b = 0; b < C::NBLK; ++b) {
+          const int wr = b * BM + row;  // row of the stage (block b)
+          const uint8_t* pk = smem + C::OFF_PK + s * C::PK_STAGE + wr * 128;
+          scv[b] = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + s * C::SC_STAGE + wr * 16);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int sub = wg + 2 * h;
+            chunk[b][2 * h] = *reinterpret_cast<const uint4*>(pk + (((2 * sub) ^ (wr & 7)) << 4));
+            chunk[b][2 * h + 1] = *reinterpret_cast<const uint4*>(pk + (((2 * sub + 1) ^ (wr & 7)) << 4));
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(w_empty(s));
@@ -305,12 +323,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int ts = tix % NT;
           if (!warp_wait(t_empty(ts), ((tix / NT) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t w[8] = {chunk[2 * h].x,     chunk[2 * h].y,     chunk[2 * h].z,     chunk[2 * h].w,
-                                 chunk[2 * h + 1].x, chunk[2 * h + 1].y, chunk[2 * h + 1].z, chunk[2 * h + 1].w};
-          const uint32_t sc = sub == 0 ? scv.x : sub == 1 ? scv.y : sub == 2 ? scv.z : scv.w;
-          uint32_t out[32];
-          dequant64(w, sc, s2, out);
-          tmem_st_32x32b_x32(tmem_base + lane_addr + A_COL + ts * 32, out);
+#pragma unroll
+          for (int b = 0; b < C::NBLK; ++b) {
+            const uint32_t w[8] = {chunk[b][2 * h].x,     chunk[b][2 * h].y,     chunk[b][2 * h].z,
+                                   chunk[b][2 * h].w,     chunk[b][2 * h + 1].x, chunk[b][2 * h + 1].y,
+                                   chunk[b][2 * h + 1].z, chunk[b][2 * h + 1].w};
+            const uint32_t sc = sub == 0 ? scv[b].x : sub == 1 ? scv[b].y : sub == 2 ? scv[b].z : scv[b].w;
+            uint32_t out[32];
+            dequant64(w, sc, s2, out);
+            tmem_st_32x32b_x32(tmem_base + lane_addr + C::A_COL + ts * 32 * C::NBLK + b * 32, out);
+          }
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
@@ -325,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int wi = 0;
       bool ok = true;
       for (int g = cid; ok && g < total; g += ncl) {
-        const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+        const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
         const CUtensorMap* mp = args.wmaps + 2 * ti.e;
         const CUtensorMap* ms = mp + 1;
         prefetch_tmap(mp);
@@ -334,8 +356,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int s = wi % C::NW;
           if (!mbar_wait(w_empty(s), ((wi / C::NW) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
           mbar_arrive_expect_tx(w_full(s), C::PK_STAGE + C::SC_STAGE);
-          tma_load_2d(sbase + C::OFF_PK + s * C::PK_STAGE, mp, ks * 128, ti.nb * BM, w_full(s));
-          tma_load_2d(sbase + C::OFF_SC + s * C::SC_STAGE, ms, ks * 16, ti.nb * BM, w_full(s));
+#pragma unroll
+          for (int b = 0; b < C::NBLK; ++b) {
+            tma_load_2d(sbase + C::OFF_PK + s * C::PK_STAGE + b * BM * 128, mp, ks * 128, (ti.nb + b) * BM, w_full(s));
+            tma_load_2d(sbase + C::OFF_SC + s * C::SC_STAGE + b * BM * 16, ms, ks * 16, (ti.nb + b) * BM, w_full(s));
+          }
         }
       }
       if (!ok)
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int ai = 0;
     bool ok = true;
     for (int g = cid; ok && g < total; g += ncl) {
-      const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+      const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
       const int ng = gathered ? (ti.bn >> 2) : (ti.bn / ID_BOX_ROWS);  // row groups per stage
       int rows[NH * 4];
 #pragma unroll
@@ -400,17 +425,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!ok && lane == 0)
       for (int j = max(0, ai - C::NA); j < ai; ++j) mbar_wait_drain(a_full(j % C::NA), (j / C::NA) & 1);
   } else {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuers
+    const int b = warp - WARP_MMA;  // weight block of this issuer
+    if (lane == 0 && b < C::NBLK) {
       int ai = 0, it = 0;
       bool ok = true;
       for (int g = cid; ok && g < total; g += ncl, ++it) {
-        const TileInfo ti = decode_tile<C::BN_MAX>(g, s_tbase, s_offs, E, CL, rank);
+        const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
         const int db = it % C::ND;
         if (!mbar_wait(d_empty(db), ((it / C::ND) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t idesc = make_idesc_bf16(BM, ti.bn);
-        const uint32_t d_tmem = tmem_base + D_COL + db * C::BN_MAX;
+        const uint32_t d_tmem = tmem_base + D_COL + (db * C::NBLK + b) * C::BN_MAX;
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % C::NA;
           const int ts = ai % NT;
@@ -418,10 +444,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!mbar_wait(t_full(ts), (ai / NT) & 1, s_abort, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t bsm = sbase + C::OFF_ACT + s * C::ACT_STAGE;
+          const uint32_t a_tmem = tmem_base + C::A_COL + ts * 32 * C::NBLK + b * 32;
 #pragma unroll
           for (int kk = 0; kk < BKA / 16; ++kk)
-            mma_bf16_ts(d_tmem, tmem_base + A_COL + ts * 32 + kk * 8, make_sdesc_sw128(bsm + kk * 32), idesc,
-                        (kb | kk) != 0);
+            mma_bf16_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(bsm + kk * 32), idesc, (kb | kk) != 0);
           if (CL > 1) mma_commit_mc(a_empty(s), mask);  // the stage is free in every CTA once all read it
           else mma_commit(a_empty(s));
           mma_commit(t_empty(ts));
@@ -429,8 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ok) mma_commit(d_full(db));
       }
       if (!ok) {
-        mma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0);
+        mma_commit(drain_bar(b));
+        mbar_wait_drain(drain_bar(b), 0);
       }
     }
   }
@@ -444,9 +470,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync_all();  // no CTA leaves while another may still multicast into it or signal it
 }
 
-using CfgS = Cfg<64, 10, 6, 2>;   // few rows per expert (HBM-bound): deep rings, small token tiles
-using CfgM = Cfg<128, 6, 5, 2>;   // ~100 rows per expert
-using CfgL = Cfg<256, 3, 4, 1>;   // hundreds of rows per expert (tensor-bound)
+// token tiles of 64 / 128 / 256 rows; the 64- and 128-row configs pair two weight blocks per CTA
+using CfgS2 = Cfg<64, 6, 4, 1, 2>;
+using CfgM2 = Cfg<128, 4, 3, 1, 2>;
+using CfgS1 = Cfg<64, 10, 6, 2, 1>;
+using CfgM1 = Cfg<128, 6, 5, 2, 1>;
+using CfgL1 = Cfg<256, 3, 4, 1, 1>;
 
 template <class C>
 int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream_t stream) {
@@ -478,7 +507,7 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream
     if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
     max_clusters[dev][lg] = n;
   }
-  const long long nbg = (args.N + BM * CL - 1) / (BM * CL);
+  const long long nbg = (args.N + BM * CL * C::NBLK - 1) / (BM * CL * C::NBLK);
   const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
   const int ncl = (int)std::max<long long>(1, std::min<long long>(max_clusters[dev][lg], max_groups));
   cfg.gridDim = dim3(ncl * CL);
@@ -486,11 +515,12 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream
   return MOE_OK;
 }
 
-// cluster width: the largest of 8, 4, 2 that divides the number of 128-row weight blocks
-int cluster_width(int N) {
+// cluster width: the largest of 8, 4, 2 that divides the number of NBLK-block groups
+int cluster_width(int N, int nblk) {
   const int nb = (N + BM - 1) / BM;
+  if (nb % nblk != 0) return 0;
   for (int c : {8, 4, 2})
-    if (nb % c == 0) return c;
+    if ((nb / nblk) % c == 0) return c;
   return 1;
 }
 
@@ -511,12 +541,18 @@ int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MOE_OK) return rc;
   }
-  const int CL = gg::cluster_width(args.N);
   // token-tile width from the mean rows per expert (the distribution itself is on the device)
   const double mean_rows = (double)args.R / args.E;
-  if (mean_rows <= 48.0) return gg::launch_cfg<gg::CfgS>(amap, args, CL, stream);
-  if (mean_rows <= 160.0) return gg::launch_cfg<gg::CfgM>(amap, args, CL, stream);
-  return gg::launch_cfg<gg::CfgL>(amap, args, CL, stream);
+  if (mean_rows <= 160.0) {
+    const int cl2 = gg::cluster_width(args.N, 2);
+    if (cl2 > 0)
+      return mean_rows <= 48.0 ? gg::launch_cfg<gg::CfgS2>(amap, args, cl2, stream)
+                               : gg::launch_cfg<gg::CfgM2>(amap, args, cl2, stream);
+    const int cl1 = gg::cluster_width(args.N, 1);
+    return mean_rows <= 48.0 ? gg::launch_cfg<gg::CfgS1>(amap, args, cl1, stream)
+                             : gg::launch_cfg<gg::CfgM1>(amap, args, cl1, stream);
+  }
+  return gg::launch_cfg<gg::CfgL1>(amap, args, gg::cluster_width(args.N, 1), stream);
 }
 
 }  // namespace moe

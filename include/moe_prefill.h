@@ -70,7 +70,7 @@ typedef enum {
  * read; the GEMMs write zeros to its output rows, which is what the pages' zeroed
  * routed-output buffer left there.
  *
- * Requirements: 1 <= E <= 1024, N % 8 == 0, 8 <= N, K % 256 == 0, K >= 256; every non-NULL
+ * Requirements: 1 <= E <= 512, N % 8 == 0, 8 <= N, K % 256 == 0, K >= 256; every non-NULL
  * packed[e] and scales[e] 16-byte aligned.  The weights are NOT copied: the table refers to
  * the caller's buffers, which must outlive it.
  *

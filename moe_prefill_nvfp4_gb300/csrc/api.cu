@@ -129,7 +129,7 @@ int moe_expert_table_create(const void* const* packed, const void* const* scales
                             int K, moe_expert_table** out) {
   if (out == nullptr || packed == nullptr || scales == nullptr || scale2 == nullptr) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
-  if (E < 1 || E > 1024 || N < 8 || N % 8 != 0 || K < 256 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (E < 1 || E > 512 || N < 8 || N % 8 != 0 || K < 256 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((long long)N * K / 2 > (1ll << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int any = 0;
   for (int e = 0; e < E; ++e) {
@@ -321,7 +321,7 @@ int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const f
 
 static bool cfg_ok(const moe_prefill_config* c) {
   return c != nullptr && c->hidden >= 256 && c->hidden % 256 == 0 && c->moe_intermediate >= 256 &&
-         c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 1024 && c->top_k >= 1 &&
+         c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 512 && c->top_k >= 1 &&
          c->top_k <= 32 && c->top_k <= c->num_experts;
 }
 

@@ -52,7 +52,7 @@ constexpr int D_COL = 0;     // accumulators first, then the A stages
 constexpr int WARP_WP = 12, WARP_AP = 13, WARP_MMA = 14;
 constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
-constexpr int MAX_E = 1024;
+constexpr int MAX_E = 512;
 constexpr int ID_BOX_ROWS = 16;  // rows per tiled box when the A rows are contiguous
 
 // BN_MAX: token-tile width (MMA N, at most 256); NA/NW: activation/weight ring depths;
@@ -69,6 +69,7 @@ struct Cfg {
   static constexpr int ROWS = BM * NBLK;
   static constexpr int A_COL = ND * NBLK * BN_MAX;
   static constexpr int NT = (TMEM_COLS - A_COL) / (32 * NBLK);
+  static constexpr bool MERGED = (NA == NT);  // one "empty" barrier per stage for SMEM and TMEM
   static constexpr int ACT_STAGE = BN_MAX * 128;
   static constexpr int PK_STAGE = ROWS * 128;
   static constexpr int SC_STAGE = ROWS * 16;
@@ -321,7 +322,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int sub = wg + 2 * h;
           const int tix = wi * 4 + sub;
           const int ts = tix % NT;
-          if (!warp_wait(t_empty(ts), ((tix / NT) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+          if (!warp_wait(C::MERGED ? a_empty(ts) : t_empty(ts), ((tix / NT) & 1) ^ 1, s_abort, args.err)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int b = 0; b < C::NBLK; ++b) {
@@ -398,16 +402,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive_expect_tx(a_full(s), ti.bn * 128);
         __syncwarp();
         const uint32_t dst0 = sbase + C::OFF_ACT + s * C::ACT_STAGE;
+        const int x = kb * BKA;
         if (gathered) {
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             const int grp = rank + CL * (lane + 32 * h);
             if (grp < ng) {
               if (CL > 1)
-                tma_gather4_mc(dst0 + grp * 512, &amap, kb * BKA, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
+                tma_gather4_mc(dst0 + grp * 512, &amap, x, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
                                rows[4 * h + 3], a_full(s), mask);
               else
-                tma_gather4(dst0 + grp * 512, &amap, kb * BKA, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
+                tma_gather4(dst0 + grp * 512, &amap, x, rows[4 * h], rows[4 * h + 1], rows[4 * h + 2],
                             rows[4 * h + 3], a_full(s));
             }
           }
@@ -415,9 +420,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int grp = rank + CL * lane; grp < ng; grp += CL * 32) {
             const int y = ti.p0 + grp * ID_BOX_ROWS;
             if (CL > 1)
-              tma_load_2d_mc(dst0 + grp * ID_BOX_ROWS * 128, &amap, kb * BKA, y, a_full(s), mask);
+              tma_load_2d_mc(dst0 + grp * ID_BOX_ROWS * 128, &amap, x, y, a_full(s), mask);
             else
-              tma_load_2d(dst0 + grp * ID_BOX_ROWS * 128, &amap, kb * BKA, y, a_full(s));
+              tma_load_2d(dst0 + grp * ID_BOX_ROWS * 128, &amap, x, y, a_full(s));
           }
         }
       }
@@ -448,9 +453,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BKA / 16; ++kk)
             mma_bf16_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(bsm + kk * 32), idesc, (kb | kk) != 0);
-          if (CL > 1) mma_commit_mc(a_empty(s), mask);  // the stage is free in every CTA once all read it
+          // One commit releases the activation slot in every CTA of the cluster; when the two
+          // rings have the same depth it also releases the TMEM A stage (the dequantisation warps
+          // then wait on the slot's barrier), otherwise a second commit does.
+          if (CL > 1) mma_commit_mc(a_empty(s), mask);
           else mma_commit(a_empty(s));
-          mma_commit(t_empty(ts));
+          if (!C::MERGED) mma_commit(t_empty(ts));
         }
         if (ok) mma_commit(d_full(db));
       }
@@ -471,16 +479,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // token tiles of 64 / 128 / 256 rows; the 64- and 128-row configs pair two weight blocks per CTA
-using CfgS2 = Cfg<64, 6, 4, 1, 2>;
-using CfgM2 = Cfg<128, 4, 3, 1, 2>;
-using CfgS1 = Cfg<64, 10, 6, 2, 1>;
-using CfgM1 = Cfg<128, 6, 5, 2, 1>;
+using CfgS2 = Cfg<64, 6, 4, 1, 2>;   // NT = 6
+using CfgM2 = Cfg<128, 4, 3, 1, 2>;  // NT = 4
+using CfgS1 = Cfg<64, 12, 6, 2, 1>;  // NT = 12
+using CfgM1 = Cfg<128, 8, 4, 2, 1>;  // NT = 8
 using CfgL1 = Cfg<256, 3, 4, 1, 1>;
 
 template <class C>
-int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream_t stream) {
+int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t stream) {
   static int configured[64] = {0};
-  static int max_clusters[64][4] = {{0}};  // per device, per log2(CL)
+  static int max_clusters[64][4] = {{0}};  // per device, per log2(cluster width)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   if (!configured[dev]) {
@@ -489,11 +497,11 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream
       return MOE_ERR_CUDA;
     configured[dev] = 1;
   }
-  const int lg = CL == 8 ? 3 : CL == 4 ? 2 : CL == 2 ? 1 : 0;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(NUM_THREADS);
@@ -501,27 +509,34 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, int CL, cudaStream
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters[dev][lg] == 0) {
-    cfg.gridDim = dim3(CL * device_sm_count());
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
-    max_clusters[dev][lg] = n;
+  // cluster width: gathered rows (TMA gather4, ~12 B/cycle/SM) want the widest multicast that
+  // divides the weight-block groups, even though 8-CTA clusters fit on only 120 of 152 SMs;
+  // contiguous rows (tiled boxes) gain nothing from it, so they use pairs.
+  const int nblocks = (args.N + BM - 1) / BM;
+  const int groups = nblocks / C::NBLK;
+  const bool gathered = args.gather != nullptr;
+  int CL = 1, ncl_max = 0;
+  for (int lg = 3; lg >= 0; --lg) {
+    const int cl = 1 << lg;
+    if (groups % cl != 0 || (!gathered && cl > 2)) continue;
+    if (max_clusters[dev][lg] == 0) {
+      attr[0].val.clusterDim.x = cl;
+      cfg.gridDim = dim3(cl * nsm);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+      max_clusters[dev][lg] = n;
+    }
+    CL = cl;
+    ncl_max = max_clusters[dev][lg];
+    break;
   }
-  const long long nbg = (args.N + BM * CL * C::NBLK - 1) / (BM * CL * C::NBLK);
+  attr[0].val.clusterDim.x = CL;
+  const long long nbg = groups / CL;
   const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
-  const int ncl = (int)std::max<long long>(1, std::min<long long>(max_clusters[dev][lg], max_groups));
+  const int ncl = (int)std::max<long long>(1, std::min<long long>(ncl_max, max_groups));
   cfg.gridDim = dim3(ncl * CL);
   if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<C>, amap, args) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
-}
-
-// cluster width: the largest of 8, 4, 2 that divides the number of NBLK-block groups
-int cluster_width(int N, int nblk) {
-  const int nb = (N + BM - 1) / BM;
-  if (nb % nblk != 0) return 0;
-  for (int c : {8, 4, 2})
-    if ((nb / nblk) % c == 0) return c;
-  return 1;
 }
 
 }  // namespace gg
@@ -541,18 +556,13 @@ int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MOE_OK) return rc;
   }
-  // token-tile width from the mean rows per expert (the distribution itself is on the device)
+  // token-tile width from the mean rows per expert (the distribution itself is on the device);
+  // two weight blocks per CTA when the number of 128-row blocks is even
   const double mean_rows = (double)args.R / args.E;
-  if (mean_rows <= 160.0) {
-    const int cl2 = gg::cluster_width(args.N, 2);
-    if (cl2 > 0)
-      return mean_rows <= 48.0 ? gg::launch_cfg<gg::CfgS2>(amap, args, cl2, stream)
-                               : gg::launch_cfg<gg::CfgM2>(amap, args, cl2, stream);
-    const int cl1 = gg::cluster_width(args.N, 1);
-    return mean_rows <= 48.0 ? gg::launch_cfg<gg::CfgS1>(amap, args, cl1, stream)
-                             : gg::launch_cfg<gg::CfgM1>(amap, args, cl1, stream);
-  }
-  return gg::launch_cfg<gg::CfgL1>(amap, args, gg::cluster_width(args.N, 1), stream);
+  const bool pairs = ((args.N + gg::BM - 1) / gg::BM) % 2 == 0;
+  if (mean_rows <= 48.0) return pairs ? gg::launch_cfg<gg::CfgS2>(amap, args, stream) : gg::launch_cfg<gg::CfgS1>(amap, args, stream);
+  if (mean_rows <= 160.0) return pairs ? gg::launch_cfg<gg::CfgM2>(amap, args, stream) : gg::launch_cfg<gg::CfgM1>(amap, args, stream);
+  return gg::launch_cfg<gg::CfgL1>(amap, args, stream);
 }
 
 }  // namespace moe

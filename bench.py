@@ -129,6 +129,49 @@ def gemm_bytes(case, off: np.ndarray, proj: str) -> int:
     return w + a_bytes + R * N * 2
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's time: every replica's timed region ends when the slowest one does."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(n_ranks: int, rows_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s of N independent replicas (weak scaling): every rank processes its own
+    chunk of `rows_per_step` rows per step; the job takes the slowest rank's time."""
+    return n_ranks * rows_per_step * steps / (max_ms / 1e3)
+
+
+GEMM_SOURCES = ("grouped_gemm.cu", "common.cuh", "internal.h")
+
+
+def measured_traffic(workload: str, launch: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
+    kernel's sources changed since those counters were taken (or the workload was not captured)."""
+    import hashlib
+
+    csrc = os.path.join(ROOT, "moe_prefill_nvfp4_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()
+    path = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if len(p) == 5 and not line.startswith("#") and p[0] == workload and p[1] == launch and p[2] == digest:
+                return int(p[3]) + int(p[4])
+    return None
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -190,12 +233,8 @@ def run_gpu(args):
         raise RuntimeError("device error during timed steps")
     step_ms = [evs[i][0].elapsed_time(evs[i][NEV - 1]) for i in range(args.steps)]
     stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(NEV - 1)] for i in range(args.steps)])
-    total_ms = float(sum(step_ms))
-    if ws_n > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = ws_n * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(float(sum(step_ms)), dev)
+    value = replica_throughput(ws_n, T, args.steps, total_ms)
 
     # ---- end to end: pinned host input -> device, forward, output -> pinned host, every step
     x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -212,11 +251,7 @@ def run_gpu(args):
         out_host.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    if ws_n > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
     h2d = x_host.numel() * 2 + (lg_host.numel() * 4 if lg_host is not None else 0)
     d2h = out_host.numel() * 2
 
@@ -232,18 +267,19 @@ def run_gpu(args):
     dname = names[dom]
     dur_s = mean_stage[dom] / 1e3
     roof = None
+    traffic = measured_traffic(args.workload, dname.replace("grouped_gemm_", "")) if dname in bytes_ else None
     if dname in bytes_:
         t_hbm = bytes_[dname] / (peaks["hbm_gbs"] * 1e9)
         t_tc = flops[dname] / (peaks["bf16_tflops"] * 1e12)
         if t_hbm >= t_tc:
             ach = bytes_[dname] / dur_s / 1e9
             roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
                     "algorithmic_bytes": bytes_[dname], "peak_source": src}
         else:
             ach = flops[dname] / dur_s / 1e12
             roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
                     "algorithmic_flops": flops[dname], "peak_source": src}
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
@@ -253,7 +289,7 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD_DESC[args.workload], "rows": T, "hidden": H, "moe_intermediate": I,
                    "experts": E, "top_k": k, "parallelism": f"replicas x{ws_n}",
                    "l2": "flushed between timed steps (256 MiB write outside the step events)"},
-        "e2e": {"value": round(ws_n * T * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(replica_throughput(ws_n, T, args.steps, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": roof,
         "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},

@@ -41,7 +41,9 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = 3,
   MOE_ERR_CUDA = 4,               /* a CUDA runtime call failed (launch, copy, attribute) */
   MOE_ERR_DEVICE = 5,             /* moe_get_device_error: a device-side check fired      */
-  MOE_ERR_NOT_BUILT_FOR_DEVICE = 6/* the current GPU is not sm_103 / sm_100 family        */
+  MOE_ERR_NOT_BUILT_FOR_DEVICE = 6,/* the current GPU is not sm_103 / sm_100 family       */
+  MOE_ERR_SCRATCH_LIMIT = 7       /* needs more than the fixed static scratch of
+                                     moe_sort_by_expert_noalloc (MOE_SORT_NOALLOC_MAX_INTS) */
 } moe_status;
 
 /* device error codes (value of *code from moe_get_device_error) */
@@ -138,6 +140,33 @@ size_t moe_sort_workspace_bytes(int T, int k, int E);
 int moe_sort_by_expert(const int32_t* ids, int T, int k, int E, int32_t* sorted_token_ids,
                        int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, void* ws,
                        size_t ws_bytes, void* stream);
+
+/*
+ * moe_sort_by_expert without a caller workspace and without allocating.  The pages describe
+ * no such call: it exists for callers that cannot hand the library scratch memory and must
+ * not allocate any -- e.g. a serving loop that froze its memory pool after warm-up, code
+ * running inside an allocator's own callback, or any place where cudaMalloc/cudaFree would be
+ * wrong because they can synchronise the device or fail under memory pressure.
+ *
+ * Same arguments, outputs, requirements and device errors as moe_sort_by_expert, minus
+ * ws/ws_bytes.  The scratch (the per-segment expert histogram, (E+1)*ceil(T*k/2048) int32) is
+ * a fixed array of MOE_SORT_NOALLOC_MAX_INTS int32 (256 KiB) in the library's own device
+ * memory, one per device, reserved when the library's device code loads; no call allocates.
+ *   - Limit: (E+1) * ceil(T*k / 2048) <= MOE_SORT_NOALLOC_MAX_INTS (e.g. E = 160: T*k up to
+ *     about 833k slots; E = 512: about 261k).  A larger problem returns MOE_ERR_SCRATCH_LIMIT
+ *     before anything is launched; use moe_sort_by_expert with a workspace instead.
+ *   - Nothing in the scratch has to start at zero: every count is written before it is read
+ *     in the same call.
+ *   - Calls that can overlap in time on one device race on the shared scratch: two streams,
+ *     or two host threads, each with a call in flight.  Calls issued in order on one stream
+ *     are safe.
+ *   - The first call on each device looks the scratch's address up (cudaGetSymbolAddress);
+ *     make that first call before any stream capture that includes this call.
+ */
+#define MOE_SORT_NOALLOC_MAX_INTS 65536
+int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t* sorted_token_ids,
+                               int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
+                               void* stream);
 
 /* ---------------------------------------------------------------- grouped W4A16 GEMM */
 /*

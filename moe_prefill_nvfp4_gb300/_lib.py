@@ -21,6 +21,7 @@ __all__ = [
     "MoeError", "lib", "load", "HEADER", "exported_names",
     "MoePrefillConfig", "WorkspaceLayout", "ExpertTable",
     "moe_router_logits", "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
+    "moe_sort_by_expert_noalloc", "MOE_SORT_NOALLOC_MAX_INTS",
     "moe_w4a16_grouped_gemm", "moe_dequant_nvfp4", "moe_swiglu_clamp", "moe_combine_indexed",
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
@@ -32,8 +33,9 @@ MOE_OK = 0
 MOE_DTYPE_BF16 = 0
 MOE_DTYPE_F32 = 1
 MOE_FWD_NUM_EVENTS = 8
+MOE_SORT_NOALLOC_MAX_INTS = 65536  # int32 entries of the library's fixed sort scratch
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
-          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_NOT_BUILT_FOR_DEVICE"}
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_NOT_BUILT_FOR_DEVICE", 7: "MOE_ERR_SCRATCH_LIMIT"}
 DEVERR = {0: "none", 1: "bad expert id", 2: "bad expert offsets", 3: "pipeline wait timeout", 4: "NaN logit",
           5: "bad gather index"}
 
@@ -75,6 +77,7 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P]),
     "moe_sort_workspace_bytes": (_SZ, [_I, _I, _I]),
     "moe_sort_by_expert": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_sort_by_expert_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_w4a16_grouped_gemm": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _I, _P]),
     "moe_dequant_nvfp4": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "moe_swiglu_clamp": (_I, [_P, _P, _I64, _I64, _I64, _P, _I64, _F, _P]),
@@ -223,6 +226,25 @@ def moe_sort_by_expert(ids: torch.Tensor, E: int, ws: Optional[torch.Tensor] = N
     _check(lib().moe_sort_by_expert(_ptr(ids), T, k, E, _ptr(out["sorted_token_ids"]), _ptr(out["sorted_expert_ids"]),
                                     _ptr(out["expert_offsets"]), _ptr(out["token_to_perm"]), _ptr(ws), ws.numel(),
                                     _stream(stream)), "moe_sort_by_expert")
+    return out
+
+
+def moe_sort_by_expert_noalloc(ids: torch.Tensor, E: int, out: Optional[dict] = None, stream=None) -> dict:
+    """moe_sort_by_expert on the library's fixed scratch (no workspace, nothing allocated by the
+    library).  `out` may hold preallocated output tensors with the keys of the returned dict."""
+    _need(ids, torch.int32, "ids")
+    T, k = ids.shape
+    R = T * k
+    dev = ids.device
+    if out is None:
+        out = dict(sorted_token_ids=torch.empty(R, dtype=torch.int32, device=dev),
+                   sorted_expert_ids=torch.empty(R, dtype=torch.int32, device=dev),
+                   expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   token_to_perm=torch.empty(T, k, dtype=torch.int32, device=dev))
+    _check(lib().moe_sort_by_expert_noalloc(_ptr(ids), T, k, E, _ptr(out["sorted_token_ids"]),
+                                            _ptr(out["sorted_expert_ids"]), _ptr(out["expert_offsets"]),
+                                            _ptr(out["token_to_perm"]), _stream(stream)),
+           "moe_sort_by_expert_noalloc")
     return out
 
 

@@ -119,6 +119,7 @@ const char* moe_status_string(int s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
     case MOE_ERR_NOT_BUILT_FOR_DEVICE: return "MOE_ERR_NOT_BUILT_FOR_DEVICE";
+    case MOE_ERR_SCRATCH_LIMIT: return "MOE_ERR_SCRATCH_LIMIT";
     default: return "MOE_ERR_UNKNOWN";
   }
 }
@@ -241,6 +242,45 @@ int moe_sort_by_expert(const int32_t* ids, int T, int k, int E, int32_t* sorted_
   if (rc != MOE_OK) return rc;
   const int R = T * k;
   int32_t* cnt = static_cast<int32_t*>(ws);
+  rc = sort_count_launch(ids, R, E, cnt, device_error_word(), as_stream(stream));
+  if (rc != MOE_OK) return rc;
+  return sort_scatter_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
+                             as_stream(stream));
+}
+
+// Fixed scratch of moe_sort_by_expert_noalloc: part of the module's device image, one copy per
+// device, so no call allocates.  Its address is looked up once per device.
+static __device__ __align__(256) int32_t g_sort_noalloc_scratch[MOE_SORT_NOALLOC_MAX_INTS];
+
+namespace {
+int32_t* g_sort_noalloc_addr[kMaxDevices] = {nullptr};
+
+int sort_noalloc_scratch(int32_t** out) {
+  const int d = current_device();
+  if (d < 0) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sort_noalloc_addr[d] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_sort_noalloc_scratch) != cudaSuccess || addr == nullptr) return MOE_ERR_CUDA;
+    g_sort_noalloc_addr[d] = static_cast<int32_t*>(addr);
+  }
+  *out = g_sort_noalloc_addr[d];
+  return MOE_OK;
+}
+}  // namespace
+
+int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t* sorted_token_ids,
+                               int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
+                               void* stream) {
+  if (!ids || !sorted_token_ids || !sorted_expert_ids || !expert_offsets || !token_to_perm) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > 32 || E < 1 || E > 1024 || (long long)T * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (sort_scratch_bytes(T * k, E) > sizeof(g_sort_noalloc_scratch)) return MOE_ERR_SCRATCH_LIMIT;
+  int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  int32_t* cnt = nullptr;
+  rc = sort_noalloc_scratch(&cnt);
+  if (rc != MOE_OK) return rc;
+  const int R = T * k;
   rc = sort_count_launch(ids, R, E, cnt, device_error_word(), as_stream(stream));
   if (rc != MOE_OK) return rc;
   return sort_scatter_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,

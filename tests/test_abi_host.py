@@ -51,6 +51,18 @@ def test_sort_rejects_and_sizes(L):
     assert L.moe_sort_by_expert(NULL, 4, 2, 8, P, P, P, P, P, 1 << 20, NULL) == 1
 
 
+def test_sort_noalloc_rejects_before_any_launch(L):
+    assert L.moe_status_string(7) == b"MOE_ERR_SCRATCH_LIMIT"
+    assert L.moe_sort_by_expert_noalloc(NULL, 4, 2, 8, P, P, P, P, NULL) == 1
+    assert L.moe_sort_by_expert_noalloc(P, 4, 33, 64, P, P, P, P, NULL) == 2  # k > 32
+    # (E+1) * ceil(T*k / 2048) int32 counts must fit the fixed 65536-entry scratch:
+    # E = 160 allows 407 segments (833,536 slots); one more slot needs 408 segments
+    assert _lib.MOE_SORT_NOALLOC_MAX_INTS == 65536
+    assert L.moe_sort_by_expert_noalloc(P, 104200, 8, 160, P, P, P, P, NULL) == 7
+    assert L.moe_sort_by_expert_noalloc(P, 833537, 1, 160, P, P, P, P, NULL) == 7
+    assert L.moe_sort_by_expert_noalloc(P, 2048, 8, 1024, P, P, P, P, NULL) != 7  # 1025 * 8 fits
+
+
 def test_gemm_and_elementwise_reject(L):
     assert L.moe_w4a16_grouped_gemm(P, 8, 256, NULL, NULL, P, 8, P, 256, 0, NULL) == 1  # no table
     assert L.moe_swiglu_clamp(P, P, 4, 12, 24, P, 12, 7.0, NULL) == 2  # width % 8

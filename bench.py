@@ -293,7 +293,9 @@ def run_gpu(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": roof,
         "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
-        "gpu_launches": (8 if wr is not None else 7) * args.steps,
+        # router (when given router weights), top-k, sort histogram + scatter, gate/up GEMM with
+        # the fused SwiGLU, down GEMM, combine
+        "gpu_launches": (7 if wr is not None else 6) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 4),
     }

@@ -191,6 +191,21 @@ int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t
                            int c_dtype, void* stream);
 
 /*
+ * The gate/up GEMM with the clamped SwiGLU fused into its epilogue ("glm5next_mlp/forward.rs"
+ * (metrale), swiglu_rows, applied to the gate/up product of the grouped-prefill arm):
+ *   act[p, j] = silu(min(g, L)) * clamp(u, -L, L),  g = C[p, j], u = C[p, I + j], j < I,
+ * with C the moe_w4a16_grouped_gemm product over a gate/up table of N = 2I rows (rows 0..I-1
+ * gate, I..2I-1 up).  g and u are the FP32 accumulators (not rounded to BF16 first);
+ * silu(z) = z / (1 + e^-z) in FP32; act is rounded to BF16 (nearest even).  The N x R
+ * product never goes to memory.  Rows of absent experts are written as zeros.
+ *   act          device BF16 [R, ld_act] (output), ld_act >= I, ld_act % 8 == 0
+ * Other arguments as moe_w4a16_grouped_gemm.  Requires W->N = 2I with I % 128 == 0.
+ */
+int moe_w4a16_grouped_gemm_swiglu(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                  const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* act,
+                                  int ld_act, float limit, void* stream);
+
+/*
  * Dequantise one expert's NVFP4 weight to a dense BF16 matrix with the grouped GEMM's own
  * device routine (for inspection and tests; the GEMMs never materialise this matrix):
  *   out[n, k] = bf16( fp32( fp32(E2M1[nibble(n, k)] * e4m3(scales[n, k/16])) * scale2 ) ).
@@ -233,7 +248,12 @@ typedef struct {
   float swiglu_limit;     /* L, e.g. 7.0 */
   int renormalize;        /* 1: renormalise the top-k weights */
   float routed_scale;     /* multiplier of the routing weights, e.g. 1.0 */
+  int flags;              /* 0, or MOE_FWD_SEPARATE_SWIGLU */
 } moe_prefill_config;
+
+/* moe_prefill_config.flags: run the SwiGLU as its own kernel on a materialised G [R, 2I]
+ * (BF16) instead of in the gate/up GEMM's epilogue (the default); for inspection and tests. */
+#define MOE_FWD_SEPARATE_SWIGLU 1
 
 /* Workspace bytes for moe_prefill_forward with up to max_rows rows (0 on a bad config). */
 size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
@@ -253,14 +273,18 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *   logits_in  device FP32 [T, E] or NULL  (exactly one of w_router / logits_in)
  *   router_bias device FP32 [E] or NULL (selection only)
  *   w_gate_up  table with E = cfg E, N = 2I, K = H;  w_down: E, N = H, K = I
- *   ws, ws_bytes device workspace >= moe_workspace_bytes(cfg, T), 256-byte aligned.  Its
+ *   ws, ws_bytes device workspace >= moe_workspace_bytes(cfg, T), 256-byte aligned (G takes
+ *              space only with MOE_FWD_SEPARATE_SWIGLU).  Its
  *              contents after the call: logits, ids, wts, the sort arrays, G, act, Y, at the
  *              offsets moe_workspace_layout reports.
  *   out        device BF16 [T, H]
  *   stage_events NULL, or a host array of MOE_FWD_NUM_EVENTS cudaEvent_t (as void*) recorded
  *              on `stream` before the first stage and after each of the 7 stages (router,
  *              top-k, sort count, sort scatter, gate/up GEMM, SwiGLU, down GEMM, combine
- *              -> events 0..7 bracket them; a skipped router records event 1 = event 0).
+ *              -> events 0..7 bracket them; a skipped router records event 1 = event 0, and
+ *              with the fused SwiGLU (the default) event 5 = event 4).
+ * The SwiGLU runs in the gate/up GEMM's epilogue (moe_w4a16_grouped_gemm_swiglu) unless
+ * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.
  */
 int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
                         const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,

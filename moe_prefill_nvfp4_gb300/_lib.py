@@ -22,7 +22,7 @@ __all__ = [
     "MoePrefillConfig", "WorkspaceLayout", "ExpertTable",
     "moe_router_logits", "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
     "moe_sort_by_expert_noalloc", "MOE_SORT_NOALLOC_MAX_INTS",
-    "moe_w4a16_grouped_gemm", "moe_dequant_nvfp4", "moe_swiglu_clamp", "moe_combine_indexed",
+    "moe_w4a16_grouped_gemm", "moe_w4a16_grouped_gemm_swiglu", "MOE_FWD_SEPARATE_SWIGLU", "moe_dequant_nvfp4", "moe_swiglu_clamp", "moe_combine_indexed",
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
 ]
@@ -33,6 +33,7 @@ MOE_OK = 0
 MOE_DTYPE_BF16 = 0
 MOE_DTYPE_F32 = 1
 MOE_FWD_NUM_EVENTS = 8
+MOE_FWD_SEPARATE_SWIGLU = 1  # moe_prefill_config.flags: SwiGLU as its own kernel on a materialised G
 MOE_SORT_NOALLOC_MAX_INTS = 65536  # int32 entries of the library's fixed sort scratch
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_NOT_BUILT_FOR_DEVICE", 7: "MOE_ERR_SCRATCH_LIMIT"}
@@ -49,7 +50,7 @@ class MoeError(RuntimeError):
 class MoePrefillConfig(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("moe_intermediate", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("swiglu_limit", ctypes.c_float), ("renormalize", ctypes.c_int),
-                ("routed_scale", ctypes.c_float)]
+                ("routed_scale", ctypes.c_float), ("flags", ctypes.c_int)]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -79,6 +80,7 @@ _SIGS = {
     "moe_sort_by_expert": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_sort_by_expert_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_w4a16_grouped_gemm": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _I, _P]),
+    "moe_w4a16_grouped_gemm_swiglu": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _F, _P]),
     "moe_dequant_nvfp4": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "moe_swiglu_clamp": (_I, [_P, _P, _I64, _I64, _I64, _P, _I64, _F, _P]),
     "moe_combine_indexed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -245,6 +247,23 @@ def moe_sort_by_expert_noalloc(ids: torch.Tensor, E: int, out: Optional[dict] = 
                                             _ptr(out["sorted_expert_ids"]), _ptr(out["expert_offsets"]),
                                             _ptr(out["token_to_perm"]), _stream(stream)),
            "moe_sort_by_expert_noalloc")
+    return out
+
+
+def moe_w4a16_grouped_gemm_swiglu(A: torch.Tensor, W: ExpertTable, expert_offsets: torch.Tensor, R: int,
+                                  limit: float = 7.0, gather_ids: Optional[torch.Tensor] = None,
+                                  out: Optional[torch.Tensor] = None, stream=None):
+    """Gate/up GEMM over a [2I, K] table with the clamped SwiGLU in its epilogue: BF16 act [R, I]."""
+    _need(A, torch.bfloat16, "A")
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    if gather_ids is not None:
+        _need(gather_ids, torch.int32, "gather_ids")
+    if out is None:
+        out = torch.empty(R, W.N // 2, dtype=torch.bfloat16, device=A.device)
+    _check(lib().moe_w4a16_grouped_gemm_swiglu(_ptr(A), A.shape[0], A.stride(0), _ptr(gather_ids), W.handle,
+                                               _ptr(expert_offsets), R, _ptr(out), out.stride(0), limit,
+                                               _stream(stream)),
+           "moe_w4a16_grouped_gemm_swiglu")
     return out
 
 

@@ -289,11 +289,18 @@ int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t*
 
 // ------------------------------------------------------------------------------------------ GEMM
 
+// swiglu_half = 0: plain GEMM into C [R, ldc >= N]; otherwise the fused SwiGLU epilogue with
+// I = swiglu_half = N / 2 writing BF16 act [R, ldc >= I].
 static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids, const moe_expert_table* W,
-                        const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st) {
+                        const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st,
+                        int swiglu_half = 0, float limit = 0.f) {
   if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
   if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (a_rows < 1 || R < 1 || lda < W->K || lda % 8 != 0 || ldc < W->N || ldc % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (swiglu_half && (c_dtype != MOE_DTYPE_BF16 || W->N != 2 * swiglu_half || swiglu_half % 128 != 0))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int out_cols = swiglu_half ? swiglu_half : W->N;
+  if (a_rows < 1 || R < 1 || lda < W->K || lda % 8 != 0 || ldc < out_cols || ldc % 8 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(A) || !aligned16(C)) return MOE_ERR_INVALID_ARG;
   int rc = ensure_device();
   if (rc != MOE_OK) return rc;
@@ -313,6 +320,8 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.ldc = ldc;
   a.c_dtype = c_dtype;
   a.err = device_error_word();
+  a.swiglu_half = swiglu_half;
+  a.limit = limit;
   return grouped_gemm_launch(a, A, a_rows, lda, st);
 }
 
@@ -320,6 +329,15 @@ int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t
                            const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
                            int c_dtype, void* stream) {
   return gemm_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, C, ldc, c_dtype, as_stream(stream));
+}
+
+int moe_w4a16_grouped_gemm_swiglu(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                  const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* act,
+                                  int ld_act, float limit, void* stream) {
+  if (W == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!(limit > 0.f)) return MOE_ERR_INVALID_ARG;
+  return gemm_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, act, ld_act, MOE_DTYPE_BF16, as_stream(stream),
+                      W->N / 2, limit);
 }
 
 int moe_dequant_nvfp4(const void* packed, const void* scales, float scale2, int N, int K, uint16_t* out,
@@ -362,7 +380,7 @@ int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const f
 static bool cfg_ok(const moe_prefill_config* c) {
   return c != nullptr && c->hidden >= 256 && c->hidden % 256 == 0 && c->moe_intermediate >= 256 &&
          c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 512 && c->top_k >= 1 &&
-         c->top_k <= 32 && c->top_k <= c->num_experts;
+         c->top_k <= 32 && c->top_k <= c->num_experts && (c->flags & ~MOE_FWD_SEPARATE_SWIGLU) == 0;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -386,7 +404,7 @@ int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspac
   L->expert_offsets = take((E + 1) * 4);
   L->token_to_perm = take(R * 4);
   L->sort_scratch = take(sort_scratch_bytes((int)R, (int)E));
-  L->G = take(R * 2 * I * 2);
+  L->G = take((c->flags & MOE_FWD_SEPARATE_SWIGLU) ? R * 2 * I * 2 : 0);
   L->act = take(R * I * 2);
   L->Y = take(R * H * 2);
   L->total = o;
@@ -454,9 +472,15 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   if ((rc = sort_count_launch(ids, R, E, cnt, err, st)) != MOE_OK) return rc;
   if ((rc = sort_scatter_launch(ids, R, k, E, cnt, sti, sei, off, t2p, st)) != MOE_OK) return rc;
   ev(3);
-  if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
-  ev(4);
-  if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
+  if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
+    if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+    ev(4);
+    if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
+  } else {
+    rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit);
+    if (rc != MOE_OK) return rc;
+    ev(4);
+  }
   ev(5);
   if ((rc = gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
   ev(6);

@@ -319,6 +319,17 @@ MOE_DEV void dequant64(const uint32_t (&w)[8], uint32_t sc, float s2, uint32_t (
 }
 
 // ------------------------------------------------------------------------------------------------
+// clamped SwiGLU of one element: silu(min(g, L)) * clamp(u, -L, L), silu(z) = z / (1 + e^-z)
+// ("glm5next_mlp/forward.rs" (metrale), swiglu_rows).  Shared by the standalone SwiGLU kernel
+// and the fused gate/up GEMM epilogue.
+
+MOE_DEV float swiglu_clamped(float g, float u, float L) {
+  const float gm = fminf(g, L);
+  const float uc = fminf(fmaxf(u, -L), L);
+  return gm / (1.0f + expf(-gm)) * uc;
+}
+
+// ------------------------------------------------------------------------------------------------
 // BF16 helpers for the SIMT kernels
 
 MOE_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

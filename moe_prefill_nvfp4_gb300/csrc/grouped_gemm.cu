@@ -120,6 +120,14 @@ MOE_DEV TileInfo decode_tile(int g, const int* s_tbase, const int* s_offs, int E
   return ti;
 }
 
+// First weight row of block b of a CTA whose first n-block is nb.  Plain GEMM: consecutive
+// blocks.  Fused SwiGLU (half = I): block 0 is gate block j = nb / 2 (rows j*128..), block 1 the
+// matching up block (rows I + j*128..), so one CTA holds both halves of 128 activation columns.
+template <int NBLK>
+MOE_DEV int weight_row(int nb, int b, int half) {
+  return half ? (nb / NBLK) * BM + b * half : (nb + b) * BM;
+}
+
 // lane 0 waits, the result is broadcast so the whole warp takes the same branch
 MOE_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
   bool ok = true;
@@ -234,8 +242,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool f32 = args.c_dtype == MOE_DTYPE_F32;
     const int esz = f32 ? 4 : 2;
     // rows of absent experts are written as zeros (the pages' zeroed routed-output rows)
+    const int out_cols = args.swiglu_half ? args.swiglu_half : args.N;
     if (!*s_bad) {
-      const int chunks_per_row = args.N * esz / 16;
+      const int chunks_per_row = out_cols * esz / 16;
       for (int e = 0; e < E; ++e) {
         if (args.packed[e] != nullptr) continue;
         for (int r = s_offs[e] + blockIdx.x; r < s_offs[e + 1]; r += gridDim.x) {
@@ -250,6 +259,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int db = it % C::ND;
       if (!warp_wait(d_full(db), (it / C::ND) & 1, s_abort, args.err)) break;
       tc_fence_after();
+      if (C::NBLK == 2 && args.swiglu_half) {
+        // fused SwiGLU: act[p, n] = silu(min(g, L)) * clamp(u, -L, L) from the FP32 accumulators
+        // of the gate block (b = 0) and the up block (b = 1); BF16 out, [R, swiglu_half]
+        const int n0 = (ti.nb / C::NBLK) * BM + q * 32;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        const uint32_t dg = D_COL + (db * C::NBLK) * C::BN_MAX;
+        const uint32_t du = dg + C::BN_MAX;
+        for (int c0 = 0; c0 < ti.cnt; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32x32b_x32(lane_base + dg + c0, g);
+          tmem_ld_32x32b_x32(lane_base + du + c0, u);
+          tmem_wait_ld();
+          if (c0 + 32 >= ti.cnt) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(d_empty(db));
+          }
+          __syncwarp();
+          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            st[j * 32 + lane] = __float2bfloat16_rn(swiglu_clamped(__uint_as_float(g[j]), __uint_as_float(u[j]), args.limit));
+          __syncwarp();
+          const int rows = min(32, ti.cnt - c0);
+          for (int c = lane; c < 32 * 4; c += 32) {
+            const int r = c >> 2, cc = c & 3;
+            if (r < rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 64 + cc * 16);
+              uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + (size_t)(ti.p0 + c0 + r) * args.ldc + n0 + cc * 8;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+        }
+        continue;
+      }
       for (int b = 0; b < C::NBLK; ++b) {
         const int n0 = (ti.nb + b) * BM + q * 32;
         const uint32_t dcol = D_COL + (db * C::NBLK + b) * C::BN_MAX;
@@ -362,8 +406,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(w_full(s), C::PK_STAGE + C::SC_STAGE);
 #pragma unroll
           for (int b = 0; b < C::NBLK; ++b) {
-            tma_load_2d(sbase + C::OFF_PK + s * C::PK_STAGE + b * BM * 128, mp, ks * 128, (ti.nb + b) * BM, w_full(s));
-            tma_load_2d(sbase + C::OFF_SC + s * C::SC_STAGE + b * BM * 16, ms, ks * 16, (ti.nb + b) * BM, w_full(s));
+            const int row = weight_row<C::NBLK>(ti.nb, b, args.swiglu_half);
+            tma_load_2d(sbase + C::OFF_PK + s * C::PK_STAGE + b * BM * 128, mp, ks * 128, row, w_full(s));
+            tma_load_2d(sbase + C::OFF_SC + s * C::SC_STAGE + b * BM * 16, ms, ks * 16, row, w_full(s));
           }
         }
       }
@@ -560,6 +605,11 @@ int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda
   // two weight blocks per CTA when the number of 128-row blocks is even
   const double mean_rows = (double)args.R / args.E;
   const bool pairs = ((args.N + gg::BM - 1) / gg::BM) % 2 == 0;
+  if (args.swiglu_half) {
+    // the fused SwiGLU needs the gate/up pair in one CTA: two-block configs only
+    if (mean_rows <= 48.0) return gg::launch_cfg<gg::CfgS2>(amap, args, stream);
+    return gg::launch_cfg<gg::CfgM2>(amap, args, stream);
+  }
   if (mean_rows <= 48.0) return pairs ? gg::launch_cfg<gg::CfgS2>(amap, args, stream) : gg::launch_cfg<gg::CfgS1>(amap, args, stream);
   if (mean_rows <= 160.0) return pairs ? gg::launch_cfg<gg::CfgM2>(amap, args, stream) : gg::launch_cfg<gg::CfgM1>(amap, args, stream);
   return gg::launch_cfg<gg::CfgL1>(amap, args, stream);

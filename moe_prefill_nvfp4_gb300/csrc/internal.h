@@ -20,6 +20,11 @@ struct GemmArgs {
   void* C;
   int E, N, K, R, a_rows, ldc, c_dtype;
   int* err;                   // device error word
+  // fused SwiGLU epilogue: 0 = plain GEMM (C is [R, N]); otherwise N = 2 * swiglu_half, the
+  // CTA pairs gate block j (weight rows j*128..) with up block j (rows swiglu_half + j*128..)
+  // and C is the BF16 activation [R, swiglu_half]
+  int swiglu_half;
+  float limit;
 };
 
 // Host: encode a tiled tensor map through the driver entry point (no libcuda link needed).

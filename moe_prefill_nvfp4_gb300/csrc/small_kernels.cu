@@ -336,12 +336,6 @@ int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* 
 // ------------------------------------------------------------------------------------------------
 // clamped SwiGLU: out = silu(min(g, L)) * clamp(u, -L, L), 8 elements per thread
 
-MOE_DEV float swiglu1(float g, float u, float L) {
-  const float gm = fminf(g, L);
-  const float uc = fminf(fmaxf(u, -L), L);
-  return gm / (1.0f + expf(-gm)) * uc;
-}
-
 __global__ void swiglu_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up, int64_t rows,
                               int64_t width, int64_t ld_in, uint16_t* __restrict__ out, int64_t ld_out, float L) {
   const int64_t vpr = width / 8;
@@ -354,7 +348,8 @@ __global__ void swiglu_kernel(const uint16_t* __restrict__ gate, const uint16_t*
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      o[i] = pack_bf16x2(swiglu1(bf16_lo(ga[i]), bf16_lo(ua[i]), L), swiglu1(bf16_hi(ga[i]), bf16_hi(ua[i]), L));
+      o[i] = pack_bf16x2(swiglu_clamped(bf16_lo(ga[i]), bf16_lo(ua[i]), L),
+                         swiglu_clamped(bf16_hi(ga[i]), bf16_hi(ua[i]), L));
     *reinterpret_cast<uint4*>(out + r * ld_out + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }

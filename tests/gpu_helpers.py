@@ -37,23 +37,25 @@ def upload(proj):
     return upload_projection(proj.packed, proj.scales, proj.scale2, proj.N, proj.K)
 
 
-def make_cfg(case) -> moe.MoePrefillConfig:
+def make_cfg(case, flags: int = 0) -> moe.MoePrefillConfig:
     return moe.MoePrefillConfig(hidden=case.H, moe_intermediate=case.I, num_experts=case.E, top_k=case.k,
                                 swiglu_limit=case.swiglu_limit, renormalize=case.renormalize,
-                                routed_scale=case.routed_scale)
+                                routed_scale=case.routed_scale, flags=flags)
 
 
 class DeviceBlock:
-    """A routed-MoE block case on the device, with one workspace."""
+    """A routed-MoE block case on the device, with one workspace.  `separate` runs the SwiGLU
+    as its own kernel on a materialised G (else it is fused into the gate/up GEMM)."""
 
-    def __init__(self, case):
+    def __init__(self, case, separate: bool = False):
         self.case = case
+        self.separate = separate
         self.x = bf16_dev(case.x)
         self.router_w = bf16_dev(case.router_w) if case.router_w is not None else None
         self.logits = torch.from_numpy(case.logits).cuda() if case.logits is not None else None
         self.gu = upload(case.gate_up)
         self.dn = upload(case.down)
-        self.cfg = make_cfg(case)
+        self.cfg = make_cfg(case, moe.MOE_FWD_SEPARATE_SWIGLU if separate else 0)
         self.layout = moe.moe_workspace_layout(self.cfg, case.T)
         self.ws = torch.empty(self.layout.total, dtype=torch.uint8, device="cuda")
         self.out = torch.empty(case.T, case.H, dtype=torch.bfloat16, device="cuda")
@@ -78,7 +80,7 @@ class DeviceBlock:
             sorted_expert_ids=self.ws_view("sorted_expert_ids", torch.int32, (R,)).cpu().numpy(),
             expert_offsets=self.ws_view("expert_offsets", torch.int32, (c.E + 1,)).cpu().numpy(),
             token_to_perm=self.ws_view("token_to_perm", torch.int32, (c.T, c.k)).cpu().numpy(),
-            G=bf16_host(self.ws_view("G", torch.bfloat16, (R, 2 * c.I))),
+            G=bf16_host(self.ws_view("G", torch.bfloat16, (R, 2 * c.I))) if self.separate else None,
             act=bf16_host(self.ws_view("act", torch.bfloat16, (R, c.I))),
             Y=bf16_host(self.ws_view("Y", torch.bfloat16, (R, c.H))),
             out=bf16_host(self.out),

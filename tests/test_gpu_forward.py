@@ -6,7 +6,9 @@ fed to the oracle's top-k, so a different summation order cannot flip a near tie
 Float stages (wts, G, act, Y, out):
 * against the BF16-rounding oracle, stage by stage: each stage's GPU output against the oracle
   applied to the same BF16 input the GPU stage consumed (G from x, act from the GPU's G, Y from
-  the GPU's act, out from the GPU's Y), within 4e-3 of max|ref|;
+  the GPU's act, out from the GPU's Y), within 4e-3 of max|ref|.  With the SwiGLU fused into
+  the gate/up GEMM (the default) G is never written: act is checked against the oracle's
+  SwiGLU of its unrounded G;
 * against the exact-FP32 oracle, as one independent chain from x to out, within 1e-2.
 A whole independent BF16 chain is not held to 4e-3: when FP32 summation order flips a BF16
 rounding of G (about 0.2% of elements), the flip propagates through act and Y, and with
@@ -48,8 +50,8 @@ def _stagewise(case, st, R):
     return act, Y, out
 
 
-def _check_full(case):
-    db = DeviceBlock(case)
+def _check_full(case, separate=False):
+    db = DeviceBlock(case, separate=separate)
     db.forward()
     torch.cuda.synchronize()
     st = db.stages()
@@ -65,20 +67,28 @@ def _check_full(case):
         np.testing.assert_array_equal(st[key], ref[key], err_msg=key)
     np.testing.assert_allclose(st["wts"], ref["wts"], rtol=2e-6, atol=1e-7)
     R = int(ref["expert_offsets"][-1])
-    act, Y, out = _stagewise(case, st, R)
-    errs = {"G": nerr(st["G"][:R], ref["G64"][:R]), "act": nerr(st["act"][:R], act), "Y": nerr(st["Y"][:R], Y),
-            "out": nerr(st["out"], out)}
+    I = case.I
+    if separate:
+        act, Y, out = _stagewise(case, st, R)
+        errs = {"G": nerr(st["G"][:R], ref["G64"][:R]), "act": nerr(st["act"][:R], act)}
+    else:
+        G = ref["G64"][:R]
+        _, Y, out = _stagewise(case, dict(st, G=np.zeros((R, 2 * I))), R)
+        errs = {"act": nerr(st["act"][:R], O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))}
+    errs.update(Y=nerr(st["Y"][:R], Y), out=nerr(st["out"], out))
     assert all(e < TOL_BF16 for e in errs.values()), ("bf16 stage-wise", errs)
     ex = chains["exact"]
+    keys = ("G", "act", "Y", "out") if separate else ("act", "Y", "out")
     chain = {k: nerr(st[k][:R] if k != "out" else st[k], ex[k + "64"][:R] if k != "out" else ex["out64"])
-             for k in ("G", "act", "Y", "out")}
+             for k in keys}
     chain_bf16 = nerr(st["out"], ref["out64"])
     assert all(e < TOL_EXACT for e in chain.values()), ("exact chain", chain, "bf16 chain out", chain_bf16)
 
 
-def test_small_ragged_block():
+@pytest.mark.parametrize("separate", [False, True], ids=["fused-swiglu", "separate-swiglu"])
+def test_small_ragged_block(separate):
     c = S.make_block_case(T=37, H=512, I=256, E=5, k=2, routing="biased", seed=31)
-    _check_full(c)
+    _check_full(c, separate)
 
 
 def test_single_row():
@@ -86,14 +96,16 @@ def test_single_row():
     _check_full(c)
 
 
-def test_absent_expert_block():
+@pytest.mark.parametrize("separate", [False, True], ids=["fused-swiglu", "separate-swiglu"])
+def test_absent_expert_block(separate):
     c = S.make_block_case(T=64, H=256, I=256, E=6, k=2, routing="biased", seed=33, absent=(2,))
-    _check_full(c)
+    _check_full(c, separate)
 
 
-def test_c1_full_chunk():
+@pytest.mark.parametrize("separate", [False, True], ids=["fused-swiglu", "separate-swiglu"])
+def test_c1_full_chunk(separate):
     """Full routed-MoE block on one 256-row chunk, with the router GEMM (H 2048, I 768, E 64)."""
-    _check_full(S.workload("c1"))
+    _check_full(S.workload("c1"), separate)
 
 
 def _check_sampled(case, tokens, variants=("bf16",)):
@@ -111,7 +123,7 @@ def _check_sampled(case, tokens, variants=("bf16",)):
     t2p = db.ws_view("token_to_perm", torch.int32, (T, k)).cpu().numpy()
     off = db.ws_view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy()
     sti = db.ws_view("sorted_token_ids", torch.int32, (R,))
-    Gd = db.ws_view("G", torch.bfloat16, (R, 2 * I))
+    Ad = db.ws_view("act", torch.bfloat16, (R, I))
     Yd = db.ws_view("Y", torch.bfloat16, (R, H))
     # routing and the sort at full size, bit-exact
     rid, rw = O.route_topk(case.logits, k)
@@ -123,27 +135,29 @@ def _check_sampled(case, tokens, variants=("bf16",)):
     np.testing.assert_array_equal(sti.cpu().numpy(), srt["sorted_token_ids"])
     nvalid = int(off[E])
     extra = [int(db.out.abs().amax(1).argmax()),
-             int(sti[int(Gd[:nvalid].abs().amax(1).argmax())]),
+             int(sti[int(Ad[:nvalid].abs().amax(1).argmax())]),
              int(sti[int(Yd[:nvalid].abs().amax(1).argmax())])]
     tokens = sorted(set(list(tokens) + extra))
     out = bf16_host(db.out[tokens])
     rows = torch.from_numpy(t2p[tokens].reshape(-1)).long().cuda()
-    G = bf16_host(Gd[rows])
     Y = bf16_host(Yd[rows])
-    A = bf16_host(db.ws_view("act", torch.bfloat16, (R, I))[rows])
-    # bf16 variant, stage by stage on the GPU's own stage inputs
+    A = bf16_host(Ad[rows])
+    # bf16 variant: act against the SwiGLU of the oracle's unrounded G (the fused epilogue never
+    # rounds G), then Y and out stage by stage on the GPU's own stage inputs
     dq = {}
     ref = O.token_forward(case, tokens, rid, rw, "bf16", dq)
-    eg = nerr(G, ref["G64"].reshape(-1, 2 * I))
-    ea = nerr(A, O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))
+    G64 = ref["G64"].reshape(-1, 2 * I)
+    ea = nerr(A, O.swiglu_clamp(G64[:, :I], G64[:, I:], case.swiglu_limit))
     ys = np.stack([A[r] @ dq["dn"](int(e)).astype(np.float64).T for r, e in enumerate(rid[tokens].reshape(-1))])
     ey = nerr(Y, ys)
     perm = np.arange(len(tokens) * k, dtype=np.int32).reshape(len(tokens), k)
     eo = nerr(out, O.combine_indexed(Y, perm, rw[tokens]))
-    assert max(eg, ea, ey, eo) < TOL_BF16, ("bf16 stage-wise", tokens, eg, ea, ey, eo)
+    assert max(ea, ey, eo) < TOL_BF16, ("bf16 stage-wise", tokens, ea, ey, eo)
     if "exact" in variants:
         ex = O.token_forward(case, tokens, rid, rw, "exact")
-        chain = (nerr(G, ex["G64"].reshape(-1, 2 * I)), nerr(Y, ex["Y64"].reshape(-1, H)), nerr(out, ex["out64"]))
+        Gx = ex["G64"].reshape(-1, 2 * I)
+        chain = (nerr(A, O.swiglu_clamp(Gx[:, :I], Gx[:, I:], case.swiglu_limit)), nerr(Y, ex["Y64"].reshape(-1, H)),
+                 nerr(out, ex["out64"]))
         assert max(chain) < TOL_EXACT, ("exact chain", tokens, chain, "bf16 chain out", nerr(out, ref["out64"]))
     db.close()
 

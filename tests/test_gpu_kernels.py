@@ -259,3 +259,38 @@ def test_gemm_each_tile_config(T, E, k, N):
     ref = _oracle_gemm(c, srt, "bf16")
     assert nerr(C.cpu().numpy().astype(np.float64), ref) < 2e-6
     proj.close()
+
+
+@pytest.mark.parametrize("T,E,k,I,big,identity", [(40, 16, 8, 256, False, False), (300, 24, 8, 256, True, False),
+                                                  (600, 4, 2, 128, True, False), (90, 12, 4, 768, False, True)],
+                         ids=["64-row", "128-row-clamped", "256-row-mean-clamped", "64-row-identity"])
+def test_gemm_swiglu_fused(T, E, k, I, big, identity):
+    """Gate/up GEMM with the clamped SwiGLU in the epilogue against the oracle's SwiGLU of the
+    unrounded BF16-operand product: act = silu(min(g, L)) * clamp(u, -L, L), L = 7.  `big`
+    scales scale2 by 200 so |g|, |u| reach past L and both clamps act."""
+    c = S.make_gemm_case(T=T, E=E, k=k, N=2 * I, K=512, seed=41 + T + I, absent=(1,))
+    if big:
+        c.w.scale2[:] = c.w.scale2 * 200.0
+    srt = moe.moe_sort_by_expert(torch.from_numpy(c.ids).cuda(), c.E)
+    proj = upload(c.w)
+    R = c.T * c.k
+    if identity:
+        A = bf16_dev(c.x)[srt["sorted_token_ids"].long()].contiguous()
+        act = moe.moe_w4a16_grouped_gemm_swiglu(A, proj.table, srt["expert_offsets"], R, limit=7.0)
+    else:
+        act = moe.moe_w4a16_grouped_gemm_swiglu(bf16_dev(c.x), proj.table, srt["expert_offsets"], R, limit=7.0,
+                                                gather_ids=srt["sorted_token_ids"])
+    torch.cuda.synchronize()
+    s = {kk: v.cpu().numpy() for kk, v in srt.items()}
+    G = _oracle_gemm(c, s, "bf16")
+    ref = O.swiglu_clamp(G[:, :I], G[:, I:], 7.0)
+    got = bf16_host(act)
+    if big:
+        assert (np.abs(G[:, :I]) > 7.0).mean() > 0.05 and (np.abs(G[:, I:]) > 7.0).mean() > 0.05
+    o = s["expert_offsets"]
+    assert (got[o[1]:o[2]] == 0).all()  # absent expert: zero rows
+    assert nerr(got, ref) < TOL_BF16
+    # per element: the BF16 rounding of act (<= 2^-9 relative) plus the FP32 summation-order
+    # difference of g and u carried through the SwiGLU
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-4 * np.abs(ref).max()).all()
+    proj.close()

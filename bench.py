@@ -200,9 +200,9 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     NEV = moe.MOE_FWD_NUM_EVENTS
 
-    def step(events=None):
+    def step(events=None, st=None):
         moe.moe_prefill_forward(cfg, x, gu.table, dn.table, ws, w_router=wr, logits=logits, out=out,
-                                stage_events=events, stream=stream)
+                                stage_events=events, stream=st if st is not None else stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -211,11 +211,52 @@ def run_gpu(args):
     if moe.moe_get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(args.steps)]
-    for row in evs:  # torch creates the CUDA event on first record; the library records it afterwards
-        for e in row:
-            e.record(stream)
+    # The forward makes no host round trip, so one chunk's whole forward is captured once into a
+    # CUDA graph and replayed per step (the launch-bound host work is paid once, as a serving
+    # loop with fixed chunk shapes does).  A second graph carries the per-stage events.
+    x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    lg_host = torch.from_numpy(case.logits).pin_memory() if case.logits is not None else None
+    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(NEV)]
+    for e in stage_ev:  # torch creates the CUDA event on first record; the library records it afterwards
+        e.record(stream)
     torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            fn(cap)
+        torch.cuda.synchronize()
+        return g
+
+    def e2e_body(st):
+        x.copy_(x_host, non_blocking=True)
+        if lg_host is not None:
+            logits.copy_(lg_host, non_blocking=True)
+        step(None, st)
+        out_host.copy_(out, non_blocking=True)
+
+    g_step = capture(lambda st: step(None, st))
+    g_stage = capture(lambda st: step(stage_ev, st))
+    g_e2e = capture(e2e_body)
+    for g in (g_step, g_stage, g_e2e):
+        for _ in range(3):
+            flush.fill_(1)
+            g.replay()
+    torch.cuda.synchronize()
+
+    def timed(run, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(1)  # L2 flush, outside the step's events
+            evs[i][0].record(stream)
+            run()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
     clocks = ClockSampler(local)
     if ws_n > 1:
         dist.barrier()
@@ -223,35 +264,27 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.3)
     t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(1)  # L2 flush, outside the step's events
-        step(evs[i])
-    torch.cuda.synchronize()
+    step_ms = timed(g_step.replay, args.steps)
     t_wall = time.perf_counter() - t_wall0
+    # per-stage times: the same graph with the stage events, one step at a time
+    stage_rows = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        g_stage.replay()
+        torch.cuda.synchronize()
+        stage_rows.append([stage_ev[j].elapsed_time(stage_ev[j + 1]) for j in range(NEV - 1)])
+    stage_ms = np.array(stage_rows)
+    # end to end: pinned host x (and logits) -> device, forward, out -> pinned host, every step
+    e2e_list = timed(g_e2e.replay, args.steps)
+    # the same forward launched eagerly from the host every step (no graph)
+    eager_list = timed(step, args.steps)
     clk = clocks.stop()
     if moe.moe_get_device_error() != 0:
         raise RuntimeError("device error during timed steps")
-    step_ms = [evs[i][0].elapsed_time(evs[i][NEV - 1]) for i in range(args.steps)]
-    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(NEV - 1)] for i in range(args.steps)])
     total_ms = max_over_ranks(float(sum(step_ms)), dev)
     value = replica_throughput(ws_n, T, args.steps, total_ms)
-
-    # ---- end to end: pinned host input -> device, forward, output -> pinned host, every step
-    x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    lg_host = torch.from_numpy(case.logits).pin_memory() if case.logits is not None else None
-    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(1)
-        e2e_ev[i][0].record(stream)
-        x.copy_(x_host, non_blocking=True)
-        if lg_host is not None:
-            logits.copy_(lg_host, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
+    e2e_ms = max_over_ranks(float(sum(e2e_list)), dev)
+    eager_ms = max_over_ranks(float(sum(eager_list)), dev)
     h2d = x_host.numel() * 2 + (lg_host.numel() * 4 if lg_host is not None else 0)
     d2h = out_host.numel() * 2
 
@@ -290,7 +323,13 @@ def run_gpu(args):
                    "experts": E, "top_k": k, "parallelism": f"replicas x{ws_n}",
                    "l2": "flushed between timed steps (256 MiB write outside the step events)"},
         "e2e": {"value": round(replica_throughput(ws_n, T, args.steps, e2e_ms), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "CUDA graph of H2D copy + moe_prefill_forward + D2H copy, replayed per step"},
+        "eager": {"value": round(replica_throughput(ws_n, T, args.steps, eager_ms), 1), "unit": "tokens/s",
+                  "ms_per_step": round(eager_ms / args.steps, 5),
+                  "how": "moe_prefill_forward launched from the host every step (no graph)"},
+        "timing": "CUDA events around each graph replay of the forward; stage_ms from a second graph with "
+                  "stage events, replayed one step at a time",
         "roofline": roof,
         "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
         # router (when given router weights), top-k, sort histogram + scatter, gate/up GEMM with

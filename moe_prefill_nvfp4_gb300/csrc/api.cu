@@ -453,8 +453,13 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   uint16_t* Y = reinterpret_cast<uint16_t*>(base + L.Y);
   const int R = T * k;
   int* err = device_error_word();
+  // inside a stream capture the events become timestamp nodes of the graph (external records)
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (stage_events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
   auto ev = [&](int i) {
-    if (stage_events && stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
+    if (stage_events && stage_events[i])
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), st,
+                               cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
   };
 
   ev(0);

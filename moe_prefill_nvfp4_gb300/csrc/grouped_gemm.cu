@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // token tiles of 64 / 128 / 256 rows; the 64- and 128-row configs pair two weight blocks per CTA
 using CfgS2 = Cfg<64, 6, 4, 1, 2>;   // NT = 6
+using CfgS2D = Cfg<64, 4, 4, 2, 2>;  // NT = 4; two accumulator buffers (contiguous rows)
 using CfgM2 = Cfg<128, 4, 3, 1, 2>;  // NT = 4
 using CfgS1 = Cfg<64, 12, 6, 2, 1>;  // NT = 12
 using CfgM1 = Cfg<128, 8, 4, 2, 1>;  // NT = 8
@@ -610,9 +611,15 @@ int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda
     if (mean_rows <= 48.0) return gg::launch_cfg<gg::CfgS2>(amap, args, stream);
     return gg::launch_cfg<gg::CfgM2>(amap, args, stream);
   }
-  if (mean_rows <= 48.0) return pairs ? gg::launch_cfg<gg::CfgS2>(amap, args, stream) : gg::launch_cfg<gg::CfgS1>(amap, args, stream);
-  if (mean_rows <= 160.0) return pairs ? gg::launch_cfg<gg::CfgM2>(amap, args, stream) : gg::launch_cfg<gg::CfgM1>(amap, args, stream);
-  return gg::launch_cfg<gg::CfgL1>(amap, args, stream);
+  // measured: gathered rows keep six activation stages at the cost of a second accumulator
+  // buffer; contiguous rows prefer the overlap of the epilogue with the next tile; above ~48 rows
+  // per expert two 128-row token tiles per weight-block pair beat one 256-row tile
+  if (mean_rows <= 48.0) {
+    if (!pairs) return gg::launch_cfg<gg::CfgS1>(amap, args, stream);
+    return gathered ? gg::launch_cfg<gg::CfgS2>(amap, args, stream) : gg::launch_cfg<gg::CfgS2D>(amap, args, stream);
+  }
+  if (pairs) return gg::launch_cfg<gg::CfgM2>(amap, args, stream);
+  return mean_rows <= 160.0 ? gg::launch_cfg<gg::CfgM1>(amap, args, stream) : gg::launch_cfg<gg::CfgL1>(amap, args, stream);
 }
 
 }  // namespace moe

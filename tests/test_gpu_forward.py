@@ -195,3 +195,24 @@ def test_forward_graph_capture_replay():
     torch.cuda.synchronize()
     assert torch.equal(db.out.view(torch.int16), eager.view(torch.int16))
     db.close()
+
+
+def test_stage_events_inside_graph_capture():
+    """Stage events recorded during capture become timestamp nodes: each replay records them."""
+    c = S.make_block_case(T=96, H=512, I=256, E=12, k=4, routing="biased", seed=35)
+    db = DeviceBlock(c)
+    s = torch.cuda.Stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_FWD_NUM_EVENTS)]
+    for e in evs:
+        e.record(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, logits=db.logits, out=db.out,
+                                stage_events=evs, stream=s)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(evs) - 1)]
+        assert all(m >= 0.0 for m in ms) and evs[0].elapsed_time(evs[-1]) > 0.0
+    db.close()

@@ -246,16 +246,20 @@ def test_gemm_deterministic_and_bad_offsets():
     proj2.close()
 
 
-@pytest.mark.parametrize("T,E,k,N", [(40, 16, 8, 512), (300, 24, 8, 512), (600, 4, 2, 512), (40, 16, 8, 384),
-                                     (300, 24, 8, 384), (90, 12, 4, 2048)],
-                         ids=["64-row-pairs", "128-row-pairs", "256-row", "64-row-odd-blocks", "128-row-odd-blocks",
+@pytest.mark.parametrize("T,E,k,N,identity", [(40, 16, 8, 512, False), (40, 16, 8, 512, True), (300, 24, 8, 512, False),
+                                              (600, 4, 2, 512, False), (40, 16, 8, 384, False),
+                                              (300, 24, 8, 384, False), (600, 4, 2, 384, False),
+                                              (90, 12, 4, 2048, False)],
+                         ids=["64-row-pairs", "64-row-pairs-2acc-contiguous", "128-row-pairs", "128-row-pairs-300-mean",
+                              "64-row-odd-blocks", "128-row-odd-blocks", "256-row-odd-blocks",
                               "64-row-pairs-cluster8"])
-def test_gemm_each_tile_config(T, E, k, N):
-    """Mean rows per expert ~20, ~100 and ~300 select the 64/128/256-row token tiles; an even
-    number of 128-row weight blocks pairs them per CTA, an odd one does not; 16 blocks make
-    clusters of 8."""
+def test_gemm_each_tile_config(T, E, k, N, identity):
+    """Mean rows per expert ~20, ~100 and ~300 with even and odd numbers of 128-row weight
+    blocks select every token-tile configuration: 64-row tiles (pairs, pairs with two
+    accumulator buffers for contiguous rows, single blocks), 128-row tiles (pairs, single
+    blocks), 256-row tiles (single blocks); 16 blocks make clusters of 8."""
     c = S.make_gemm_case(T=T, E=E, k=k, N=N, K=512, seed=23 + T + N)
-    C, srt, proj = _gemm_case(c)
+    C, srt, proj = _gemm_case(c, identity=identity)
     ref = _oracle_gemm(c, srt, "bf16")
     assert nerr(C.cpu().numpy().astype(np.float64), ref) < 2e-6
     proj.close()

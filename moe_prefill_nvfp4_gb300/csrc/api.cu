@@ -242,10 +242,8 @@ int moe_sort_by_expert(const int32_t* ids, int T, int k, int E, int32_t* sorted_
   if (rc != MOE_OK) return rc;
   const int R = T * k;
   int32_t* cnt = static_cast<int32_t*>(ws);
-  rc = sort_count_launch(ids, R, E, cnt, device_error_word(), as_stream(stream));
-  if (rc != MOE_OK) return rc;
-  return sort_scatter_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
-                             as_stream(stream));
+  return sort_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
+                     device_error_word(), as_stream(stream));
 }
 
 // Fixed scratch of moe_sort_by_expert_noalloc: part of the module's device image, one copy per
@@ -281,10 +279,8 @@ int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t*
   rc = sort_noalloc_scratch(&cnt);
   if (rc != MOE_OK) return rc;
   const int R = T * k;
-  rc = sort_count_launch(ids, R, E, cnt, device_error_word(), as_stream(stream));
-  if (rc != MOE_OK) return rc;
-  return sort_scatter_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
-                             as_stream(stream));
+  return sort_launch(ids, R, k, E, cnt, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm,
+                     device_error_word(), as_stream(stream));
 }
 
 // ------------------------------------------------------------------------------------------ GEMM
@@ -474,8 +470,7 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
       MOE_OK)
     return rc;
   ev(2);
-  if ((rc = sort_count_launch(ids, R, E, cnt, err, st)) != MOE_OK) return rc;
-  if ((rc = sort_scatter_launch(ids, R, k, E, cnt, sti, sei, off, t2p, st)) != MOE_OK) return rc;
+  if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st)) != MOE_OK) return rc;
   ev(3);
   if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
     if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;

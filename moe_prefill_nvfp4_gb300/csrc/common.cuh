@@ -319,6 +319,15 @@ MOE_DEV void dequant64(const uint32_t (&w)[8], uint32_t sc, float s2, uint32_t (
 }
 
 // ------------------------------------------------------------------------------------------------
+// programmatic dependent launch: kernels launched with programmatic stream serialization may
+// start before the previous kernel of the stream has finished.  griddep_wait() blocks until that
+// kernel has completed and its memory is visible (a no-op without the launch attribute);
+// griddep_launch_dependents() lets the next kernel be scheduled (it still waits for our end).
+
+MOE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------------------
 // clamped SwiGLU of one element: silu(min(g, L)) * clamp(u, -L, L), silu(z) = z / (1 + e^-z)
 // ("glm5next_mlp/forward.rs" (metrale), swiglu_rows).  Shared by the standalone SwiGLU kernel
 // and the fused gate/up GEMM epilogue.

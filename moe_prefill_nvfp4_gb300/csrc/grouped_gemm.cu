@@ -194,6 +194,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
     tmem_relinquish();
   }
+  // everything above overlaps the previous kernel of the stream; its outputs are read below
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = tid; i <= E; i += NUM_THREADS) s_offs[i] = args.offsets[i];
   __syncthreads();
 
@@ -546,15 +549,17 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   const int nsm = device_sm_count();
   if (nsm <= 0) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = C::SMEM_ALLOC;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy queries below take the cluster attribute alone
   // cluster width: gathered rows (TMA gather4, ~12 B/cycle/SM) want the widest multicast that
   // divides the weight-block groups, even though 8-CTA clusters fit on only 120 of 152 SMs;
   // contiguous rows (tiled boxes) gain nothing from it, so they use pairs.
@@ -581,6 +586,7 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);
   const int ncl = (int)std::max<long long>(1, std::min<long long>(ncl_max, max_groups));
   cfg.gridDim = dim3(ncl * CL);
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<C>, amap, args) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

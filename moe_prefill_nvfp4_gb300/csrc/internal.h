@@ -36,16 +36,34 @@ int* device_error_word();  // device address of the current device's error word
 
 int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda, cudaStream_t stream);
 
+// Launch with programmatic stream serialization (the kernel calls griddep_wait() before it reads
+// what earlier work in the stream wrote).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // SIMT kernels (small_kernels.cu)
 int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st);
 int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
                       int32_t* ids, float* wts, int* err, cudaStream_t st);
 int sort_segments(int R, int E);
 size_t sort_scratch_bytes(int R, int E);
-int sort_count_launch(const int32_t* ids, int R, int E, int32_t* cnt, int* err, cudaStream_t st);
-int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* cnt, int32_t* sorted_token_ids,
-                        int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
-                        cudaStream_t st);
+// The stable sort: one block when R <= 2048 (cnt unused), else histogram + scatter kernels over
+// segments of 2048 slots with the per-segment counts in cnt (sort_scratch_bytes).
+int sort_launch(const int32_t* ids, int R, int k, int E, int32_t* cnt, int32_t* sorted_token_ids,
+                int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, int* err,
+                cudaStream_t st);
 int swiglu_launch(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in, uint16_t* out,
                   int64_t ld_out, float limit, cudaStream_t st);
 int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, const uint16_t* shared_out, int T, int k,

@@ -19,63 +19,76 @@ namespace moe {
 // ------------------------------------------------------------------------------------------------
 // router logits: logits[t, e] = sum_h x[t, h] * w[e, h]  (BF16 in, FP32 accumulate and out)
 //
-// A warp owns a 4-token x 8-expert block; lanes split h in 8-element vectors, each lane keeps
-// 32 FP32 partial sums, then a fixed xor-butterfly reduces them (deterministic order).
+// A block owns a 4-token x 8-expert tile and its 8 warps split h: every lane loads one 16-byte
+// vector of each of the 12 rows per 2048 h up front (one memory round trip), keeps 32 FP32
+// partial sums, and the 32 sums are reduce-scattered across the warp (lane j ends with output
+// j) and then added over the warps in a fixed order: deterministic.
 
-constexpr int RL_TOK = 4, RL_EXP = 8, RL_WARPS = 4;
+constexpr int RL_TOK = 4, RL_EXP = 8, RL_WARPS = 8;
 
 __global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint16_t* __restrict__ x,
                                                                       const uint16_t* __restrict__ w, int T, int H,
                                                                       int E, float* __restrict__ logits) {
+  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * RL_TOK;
-  const int e0 = (blockIdx.y * RL_WARPS + warp) * RL_EXP;
-  if (e0 >= E) return;
-  float acc[RL_TOK][RL_EXP];
+  const int e0 = blockIdx.y * RL_EXP;
+  float v[RL_TOK * RL_EXP];
 #pragma unroll
-  for (int i = 0; i < RL_TOK; ++i)
-#pragma unroll
-    for (int j = 0; j < RL_EXP; ++j) acc[i][j] = 0.f;
+  for (int i = 0; i < RL_TOK * RL_EXP; ++i) v[i] = 0.f;
   const int nvec = H / 8;
-  for (int v = lane; v < nvec; v += 32) {
+  for (int vi = threadIdx.x; vi < nvec; vi += RL_WARPS * 32) {
     uint4 xv[RL_TOK], wv[RL_EXP];
 #pragma unroll
     for (int i = 0; i < RL_TOK; ++i)
-      xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + v) : make_uint4(0, 0, 0, 0);
+      xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + vi) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int j = 0; j < RL_EXP; ++j)
-      wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + j) * H) + v) : make_uint4(0, 0, 0, 0);
+      wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + j) * H) + vi) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < RL_TOK; ++i) {
       const uint32_t xa[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
       for (int j = 0; j < RL_EXP; ++j) {
         const uint32_t wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-        float a = acc[i][j];
+        float a = v[i * RL_EXP + j];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           a = fmaf(bf16_lo(xa[c]), bf16_lo(wa[c]), a);
           a = fmaf(bf16_hi(xa[c]), bf16_hi(wa[c]), a);
         }
-        acc[i][j] = a;
+        v[i * RL_EXP + j] = a;
       }
     }
   }
+  // reduce-scatter of the 32 sums over the warp: after the step with offset o a lane keeps the
+  // half of its values selected by its lane bit o and adds the partner's copy of that half
 #pragma unroll
-  for (int i = 0; i < RL_TOK; ++i)
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
 #pragma unroll
-    for (int j = 0; j < RL_EXP; ++j) {
-      float a = acc[i][j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == ((i * RL_EXP + j) & 31) && t0 + i < T && e0 + j < E) logits[(size_t)(t0 + i) * E + e0 + j] = a;
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
+  }
+  s_red[warp][lane] = v[0];  // output index lane = i * RL_EXP + j
+  __syncthreads();
+  if (threadIdx.x < RL_TOK * RL_EXP) {
+    float a = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < RL_WARPS; ++ww) a += s_red[ww][threadIdx.x];
+    const int i = threadIdx.x / RL_EXP, j = threadIdx.x % RL_EXP;
+    if (t0 + i < T && e0 + j < E) logits[(size_t)(t0 + i) * E + e0 + j] = a;
+  }
 }
 
 int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st) {
-  dim3 grid((T + RL_TOK - 1) / RL_TOK, (E + RL_EXP * RL_WARPS - 1) / (RL_EXP * RL_WARPS));
-  router_logits_kernel<<<grid, RL_WARPS * 32, 0, st>>>(x, w, T, H, E, logits);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  dim3 grid((T + RL_TOK - 1) / RL_TOK, (E + RL_EXP - 1) / RL_EXP);
+  return launch_pdl(router_logits_kernel, grid, dim3(RL_WARPS * 32), 0, st, x, w, T, H, E, logits);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -90,6 +103,8 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32)
     route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
                       int renormalize, float routed_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
                       int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * TOPK_WARPS + warp;
   if (row >= T) return;
@@ -170,15 +185,15 @@ int route_topk_launch(const float* logits, const float* bias, int T, int E, int 
   const int grid = (T + TOPK_WARPS - 1) / TOPK_WARPS;
   const int npl = (E + 31) / 32;
 #define MOE_TOPK_CASE(N)                                                                                  \
-  route_topk_kernel<N><<<grid, TOPK_WARPS * 32, 0, st>>>(logits, bias, T, E, k, renormalize, scale, ids, wts, err)
-  if (npl <= 1) MOE_TOPK_CASE(1);
-  else if (npl <= 2) MOE_TOPK_CASE(2);
-  else if (npl <= 4) MOE_TOPK_CASE(4);
-  else if (npl <= 8) MOE_TOPK_CASE(8);
-  else if (npl <= 16) MOE_TOPK_CASE(16);
-  else MOE_TOPK_CASE(32);
+  launch_pdl(route_topk_kernel<N>, dim3(grid), dim3(TOPK_WARPS * 32), 0, st, logits, bias, T, E, k, renormalize, \
+             scale, ids, wts, err)
+  if (npl <= 1) return MOE_TOPK_CASE(1);
+  if (npl <= 2) return MOE_TOPK_CASE(2);
+  if (npl <= 4) return MOE_TOPK_CASE(4);
+  if (npl <= 8) return MOE_TOPK_CASE(8);
+  if (npl <= 16) return MOE_TOPK_CASE(16);
+  return MOE_TOPK_CASE(32);
 #undef MOE_TOPK_CASE
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -208,6 +223,8 @@ MOE_DEV int bucket_of(int id, int E) { return (id >= 0 && id < E) ? id : E; }
 __global__ void __launch_bounds__(SORT_THREADS)
     sort_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int S, int32_t* __restrict__ cnt, int* err) {
   extern __shared__ int s_hist[];
+  griddep_wait();
+  griddep_launch_dependents();
   const int seg = blockIdx.x;
   for (int b = threadIdx.x; b <= E; b += SORT_THREADS) s_hist[b] = 0;
   __syncthreads();
@@ -227,6 +244,8 @@ __global__ void __launch_bounds__(SORT_THREADS)
                         int32_t* __restrict__ sorted_token_ids, int32_t* __restrict__ sorted_expert_ids,
                         int32_t* __restrict__ expert_offsets, int32_t* __restrict__ token_to_perm) {
   extern __shared__ int s_mem[];
+  griddep_wait();
+  griddep_launch_dependents();
   const int NB = E + 1;
   int* s_base = s_mem;                                              // [NB]
   int16_t* s_wcnt = reinterpret_cast<int16_t*>(s_base + NB);        // [SORT_WARPS][NB]
@@ -234,6 +253,14 @@ __global__ void __launch_bounds__(SORT_THREADS)
   int16_t* s_bkt = s_lpos + SORT_SEG;                               // [SORT_SEG]
   const int seg = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // this lane's slots, loaded first so their latency overlaps the bucket prefix below
+  const int lo = seg * SORT_SEG, hi = min(R, lo + SORT_SEG);
+  int bk[SORT_PER_WARP / 32];
+#pragma unroll
+  for (int c = 0; c < SORT_PER_WARP / 32; ++c) {
+    const int i = lo + warp * SORT_PER_WARP + c * 32 + lane;
+    bk[c] = i < hi ? bucket_of(ids[i], E) : -1;
+  }
 
   // (1) total slots per bucket over all segments
   for (int b = tid; b < NB; b += SORT_THREADS) {
@@ -273,13 +300,12 @@ __global__ void __launch_bounds__(SORT_THREADS)
   __syncthreads();
 
   // (2) stable ranks inside the segment
-  const int lo = seg * SORT_SEG, hi = min(R, lo + SORT_SEG);
   const uint32_t lt = (1u << lane) - 1u;
   int16_t* wc = s_wcnt + warp * NB;
+#pragma unroll
   for (int c = 0; c < SORT_PER_WARP; c += 32) {
     const int li = warp * SORT_PER_WARP + c + lane;  // slot index inside the segment
-    const int i = lo + li;
-    const int b = i < hi ? bucket_of(ids[i], E) : -1;
+    const int b = bk[c / 32];
     const uint32_t peers = __match_any_sync(0xffffffffu, b);
     int local = 0;
     if (b >= 0) local = wc[b] + __popc(peers & lt);
@@ -313,24 +339,107 @@ __global__ void __launch_bounds__(SORT_THREADS)
   }
 }
 
+// R <= SORT_SEG: one block does the whole sort (histogram, bucket prefix, stable ranks and the
+// writes) with the counts in shared memory: no scratch, one launch.
+__global__ void __launch_bounds__(SORT_THREADS)
+    sort_single_kernel(const int32_t* __restrict__ ids, int R, int k, int E, int32_t* __restrict__ sorted_token_ids,
+                       int32_t* __restrict__ sorted_expert_ids, int32_t* __restrict__ expert_offsets,
+                       int32_t* __restrict__ token_to_perm, int* err) {
+  extern __shared__ int s_mem[];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int NB = E + 1;
+  int* s_base = s_mem;                                              // [NB]
+  int16_t* s_wcnt = reinterpret_cast<int16_t*>(s_base + NB);        // [SORT_WARPS][NB]
+  int16_t* s_lpos = s_wcnt + SORT_WARPS * NB;                       // [SORT_SEG]
+  int16_t* s_bkt = s_lpos + SORT_SEG;                               // [SORT_SEG]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int bk[SORT_PER_WARP / 32];
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < SORT_PER_WARP / 32; ++c) {
+    const int i = warp * SORT_PER_WARP + c * 32 + lane;
+    const int id = i < R ? ids[i] : -1;
+    if (i < R && (id < -1 || id >= E)) bad = true;
+    bk[c] = i < R ? bucket_of(id, E) : -1;
+  }
+  for (int i = tid; i < SORT_WARPS * NB; i += SORT_THREADS) s_wcnt[i] = 0;
+  if (__syncthreads_or(bad) && tid == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
+  // stable ranks inside each warp's run of slots, per-warp bucket counts
+  const uint32_t lt = (1u << lane) - 1u;
+  int16_t* wc = s_wcnt + warp * NB;
+#pragma unroll
+  for (int c = 0; c < SORT_PER_WARP / 32; ++c) {
+    const int li = warp * SORT_PER_WARP + c * 32 + lane;
+    const int b = bk[c];
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    int local = 0;
+    if (b >= 0) local = wc[b] + __popc(peers & lt);
+    __syncwarp();
+    if (b >= 0 && (__ffs(peers) - 1) == lane) wc[b] = (int16_t)(wc[b] + __popc(peers));
+    __syncwarp();
+    s_lpos[li] = (int16_t)local;
+    s_bkt[li] = (int16_t)b;
+  }
+  __syncthreads();
+  // per bucket: exclusive prefix over the warps, and the bucket total
+  for (int b = tid; b < NB; b += SORT_THREADS) {
+    int run = 0;
+    for (int w = 0; w < SORT_WARPS; ++w) {
+      const int t = s_wcnt[w * NB + b];
+      s_wcnt[w * NB + b] = (int16_t)run;
+      run += t;
+    }
+    s_base[b] = run;
+  }
+  __syncthreads();
+  // exclusive prefix of the totals over buckets (warp 0: each lane a contiguous run)
+  if (warp == 0) {
+    const int per = (NB + 31) / 32;
+    const int b0 = min(NB, lane * per), b1 = min(NB, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += s_base[b];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int b = b0; b < b1; ++b) {
+      const int t = s_base[b];
+      s_base[b] = run;
+      expert_offsets[b] = run;  // b == E: number of valid slots
+      run += t;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < R; i += SORT_THREADS) {
+    const int b = s_bkt[i];
+    const int p = s_base[b] + s_wcnt[(i / SORT_PER_WARP) * NB + b] + s_lpos[i];
+    sorted_token_ids[p] = i / k;
+    sorted_expert_ids[p] = b < E ? b : -1;
+    token_to_perm[i] = b < E ? p : -1;
+  }
+}
+
 static size_t scatter_smem(int E) {
   const int NB = E + 1;
   return (size_t)NB * 4 + (size_t)SORT_WARPS * NB * 2 + (size_t)SORT_SEG * 2 * 2;
 }
 
-int sort_count_launch(const int32_t* ids, int R, int E, int32_t* cnt, int* err, cudaStream_t st) {
+int sort_launch(const int32_t* ids, int R, int k, int E, int32_t* cnt, int32_t* sorted_token_ids,
+                int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, int* err,
+                cudaStream_t st) {
+  if (R <= SORT_SEG)
+    return launch_pdl(sort_single_kernel, dim3(1), dim3(SORT_THREADS), scatter_smem(E), st, ids, R, k, E,
+                      sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, err);
   const int S = sort_segments(R, E);
-  sort_hist_kernel<<<S, SORT_THREADS, (E + 1) * sizeof(int), st>>>(ids, R, E, S, cnt, err);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* cnt, int32_t* sorted_token_ids,
-                        int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm,
-                        cudaStream_t st) {
-  const int S = sort_segments(R, E);
-  sort_scatter_kernel<<<S, SORT_THREADS, scatter_smem(E), st>>>(ids, R, k, E, S, cnt, sorted_token_ids,
-                                                               sorted_expert_ids, expert_offsets, token_to_perm);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int rc = launch_pdl(sort_hist_kernel, dim3(S), dim3(SORT_THREADS), (E + 1) * sizeof(int), st, ids, R, E, S,
+                            cnt, err);
+  if (rc != MOE_OK) return rc;
+  return launch_pdl(sort_scatter_kernel, dim3(S), dim3(SORT_THREADS), scatter_smem(E), st, ids, R, k, E, S, cnt,
+                    sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -338,6 +447,8 @@ int sort_scatter_launch(const int32_t* ids, int R, int k, int E, const int32_t* 
 
 __global__ void swiglu_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up, int64_t rows,
                               int64_t width, int64_t ld_in, uint16_t* __restrict__ out, int64_t ld_out, float L) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t vpr = width / 8;
   const int64_t total = rows * vpr;
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -360,63 +471,72 @@ int swiglu_launch(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_
   if (total == 0) return MOE_OK;
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, (int64_t)device_sm_count() * 16);
-  swiglu_kernel<<<(int)blocks, threads, 0, st>>>(gate, up, rows, width, ld_in, out, ld_out, limit);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(swiglu_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, gate, up, rows, width, ld_in, out,
+                    ld_out, limit);
 }
 
 // ------------------------------------------------------------------------------------------------
 // indexed combine: out[t] = sum_s wts[t, s] * Y[token_to_perm[t, s]] (+ shared_out[t]), slot order
+//
+// One thread per (token, 8-column vector).  The slots are taken 8 at a time with all 8 row loads
+// issued before the FP32 accumulation, which stays in slot order (deterministic).
 
-constexpr int CMB_THREADS = 128;
+constexpr int CMB_THREADS = 256;
+constexpr int CMB_BATCH = 8;
 
 __global__ void __launch_bounds__(CMB_THREADS)
     combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ perm, const float* __restrict__ wts,
-                   const uint16_t* __restrict__ shared_out, int k, int H, uint16_t* __restrict__ out) {
-  __shared__ int s_perm[32];
-  __shared__ float s_w[32];
-  const int t = blockIdx.x;
-  if (threadIdx.x < k) {
-    s_perm[threadIdx.x] = perm[(size_t)t * k + threadIdx.x];
-    s_w[threadIdx.x] = wts[(size_t)t * k + threadIdx.x];
-  }
-  __syncthreads();
+                   const uint16_t* __restrict__ shared_out, int T, int k, int H, uint16_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int nvec = H / 8;
-  for (int v = threadIdx.x; v < nvec; v += CMB_THREADS) {
-    float acc[8];
+  const int64_t g = (int64_t)blockIdx.x * CMB_THREADS + threadIdx.x;
+  if (g >= (int64_t)T * nvec) return;
+  const int t = (int)(g / nvec), v = (int)(g - (int64_t)t * nvec);
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int s = 0; s < k; ++s) {
-      const int p = s_perm[s];
-      if (p < 0) continue;
-      const float w = s_w[s];
-      const uint4 y = *reinterpret_cast<const uint4*>(Y + (size_t)p * H + v * 8);
-      const uint32_t ya[4] = {y.x, y.y, y.z, y.w};
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int s0 = 0; s0 < k; s0 += CMB_BATCH) {
+    uint4 y[CMB_BATCH];
+    float w[CMB_BATCH];
+#pragma unroll
+    for (int j = 0; j < CMB_BATCH; ++j) {
+      const int s = s0 + j;
+      const int p = s < k ? __ldg(perm + (size_t)t * k + s) : -1;
+      w[j] = s < k ? __ldg(wts + (size_t)t * k + s) : 0.f;
+      y[j] = p >= 0 ? __ldg(reinterpret_cast<const uint4*>(Y + (size_t)p * H) + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < CMB_BATCH; ++j) {
+      if (s0 + j >= k) break;
+      const uint32_t ya[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(w, bf16_lo(ya[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(w, bf16_hi(ya[i]), acc[2 * i + 1]);
+        acc[2 * i] = fmaf(w[j], bf16_lo(ya[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w[j], bf16_hi(ya[i]), acc[2 * i + 1]);
       }
     }
-    if (shared_out) {
-      const uint4 y = *reinterpret_cast<const uint4*>(shared_out + (size_t)t * H + v * 8);
-      const uint32_t ya[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] += bf16_lo(ya[i]);
-        acc[2 * i + 1] += bf16_hi(ya[i]);
-      }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
-    *reinterpret_cast<uint4*>(out + (size_t)t * H + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (shared_out) {
+    const uint4 y = __ldg(reinterpret_cast<const uint4*>(shared_out + (size_t)t * H) + v);
+    const uint32_t ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += bf16_lo(ya[i]);
+      acc[2 * i + 1] += bf16_hi(ya[i]);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, const uint16_t* shared_out, int T, int k,
                    int H, uint16_t* out, cudaStream_t st) {
-  combine_kernel<<<T, CMB_THREADS, 0, st>>>(Y, perm, wts, shared_out, k, H, out);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int64_t total = (int64_t)T * (H / 8);
+  return launch_pdl(combine_kernel, dim3((unsigned)((total + CMB_THREADS - 1) / CMB_THREADS)), dim3(CMB_THREADS), 0, st,
+                    Y, perm, wts, shared_out, T, k, H, out);
 }
 
 // ------------------------------------------------------------------------------------------------

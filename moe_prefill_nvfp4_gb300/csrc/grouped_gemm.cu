@@ -537,7 +537,7 @@ using CfgL1 = Cfg<256, 3, 4, 1, 1>;
 template <class C>
 int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t stream) {
   static int configured[64] = {0};
-  static int max_clusters[64][4] = {{0}};  // per device, per log2(cluster width)
+  static int max_clusters[64][9] = {{0}};  // per device, per cluster width
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   if (!configured[dev]) {
@@ -560,25 +560,24 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy queries below take the cluster attribute alone
-  // cluster width: gathered rows (TMA gather4, ~12 B/cycle/SM) want the widest multicast that
-  // divides the weight-block groups, even though 8-CTA clusters fit on only 120 of 152 SMs;
-  // contiguous rows (tiled boxes) gain nothing from it, so they use pairs.
+  // cluster width: gathered rows are bound by the TMA gather4 issue rate of each SM (~80-150
+  // cycles per 4-row copy), so they take the widest multicast (any width up to 8, not only powers
+  // of two) that divides the weight-block groups; contiguous rows in tiled boxes use pairs.
   const int nblocks = (args.N + BM - 1) / BM;
   const int groups = nblocks / C::NBLK;
   const bool gathered = args.gather != nullptr;
   int CL = 1, ncl_max = 0;
-  for (int lg = 3; lg >= 0; --lg) {
-    const int cl = 1 << lg;
-    if (groups % cl != 0 || (!gathered && cl > 2)) continue;
-    if (max_clusters[dev][lg] == 0) {
+  for (int cl = gathered ? 8 : 2; cl >= 1; --cl) {
+    if (groups % cl != 0) continue;
+    if (max_clusters[dev][cl] == 0) {
       attr[0].val.clusterDim.x = cl;
       cfg.gridDim = dim3(cl * nsm);
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
-      max_clusters[dev][lg] = n;
+      max_clusters[dev][cl] = n;
     }
     CL = cl;
-    ncl_max = max_clusters[dev][lg];
+    ncl_max = max_clusters[dev][cl];
     break;
   }
   attr[0].val.clusterDim.x = CL;

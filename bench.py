@@ -117,16 +117,17 @@ def build_case(name: str):
 
 def gemm_bytes(case, off: np.ndarray, proj: str) -> int:
     """Algorithmic bytes of one grouped GEMM launch: every touched expert's packed weights and
-    scales once (+ its scale2), the unique A rows, and C written once."""
+    scales once (+ its scale2), the unique A rows, and the output written once (the gate/up
+    launch writes the SwiGLU activation [R, I] from its epilogue, not G [R, 2I])."""
     E = case.E
     touched = int((np.diff(off[:E + 1]) > 0).sum())
     R = int(off[E])
     if proj == "gate_up":
-        N, K, a_bytes = 2 * case.I, case.H, case.T * case.H * 2
+        N, K, a_bytes, c_bytes = 2 * case.I, case.H, case.T * case.H * 2, R * case.I * 2
     else:
-        N, K, a_bytes = case.H, case.I, R * case.I * 2
+        N, K, a_bytes, c_bytes = case.H, case.I, R * case.I * 2, R * case.H * 2
     w = touched * (N * K // 2 + N * K // 16 + 4)
-    return w + a_bytes + R * N * 2
+    return w + a_bytes + c_bytes
 
 
 def max_over_ranks(x: float, device) -> float:

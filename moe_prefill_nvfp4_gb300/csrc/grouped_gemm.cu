@@ -561,12 +561,16 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy queries below take the cluster attribute alone
   // cluster width: gathered rows are bound by the TMA gather4 issue rate of each SM (~80-150
-  // cycles per 4-row copy), so they take the widest multicast (any width up to 8, not only powers
-  // of two) that divides the weight-block groups; contiguous rows in tiled boxes use pairs.
+  // cycles per 4-row copy), so wider multicast (any width up to 8 that divides the weight-block
+  // groups, not only powers of two) makes each tile cheaper; but wide clusters leave SMs idle
+  // (8-CTA clusters fit on 120 of 152 SMs, 6-CTA on 138), which costs a whole tile round when
+  // there are few rounds.  So: the widest width whose clusters cover >= 94% of the SMs, unless
+  // the launch has many tile rounds (>= 24 expected), where the widest width wins.  Contiguous
+  // rows in tiled boxes use pairs.
   const int nblocks = (args.N + BM - 1) / BM;
   const int groups = nblocks / C::NBLK;
   const bool gathered = args.gather != nullptr;
-  int CL = 1, ncl_max = 0;
+  int CL = 1, ncl_max = 0, widest = 0;
   for (int cl = gathered ? 8 : 2; cl >= 1; --cl) {
     if (groups % cl != 0) continue;
     if (max_clusters[dev][cl] == 0) {
@@ -576,10 +580,21 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
       if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
       max_clusters[dev][cl] = n;
     }
-    CL = cl;
-    ncl_max = max_clusters[dev][cl];
-    break;
+    const int ctas = max_clusters[dev][cl] * cl;
+    if (widest == 0) {
+      widest = cl;
+      const double rounds = (double)groups * ((args.R + C::BN_MAX - 1) / C::BN_MAX) / ctas;
+      if (rounds >= 24.0) {
+        CL = cl;
+        break;
+      }
+    }
+    if (ctas * 100 >= nsm * 94) {
+      CL = cl;
+      break;
+    }
   }
+  ncl_max = max_clusters[dev][CL];
   attr[0].val.clusterDim.x = CL;
   const long long nbg = groups / CL;
   const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);

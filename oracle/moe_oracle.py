@@ -49,6 +49,7 @@ __all__ = [
     "grouped_gemm",
     "swiglu_clamp",
     "combine_indexed",
+    "shared_expert_mlp",
     "prefill_forward",
     "token_forward",
     "VARIANTS",
@@ -320,6 +321,30 @@ def combine_indexed(y: np.ndarray, token_to_perm: np.ndarray, wts: np.ndarray,
 # whole path
 
 
+def shared_expert_mlp(x_bits: np.ndarray, shared, limit: float, variant: str = "bf16") -> Dict[str, np.ndarray]:
+    """The shared expert over every row: a dense SwiGLU MLP with BF16 weights.
+
+    [fwd-old] ``forward_dense``: ``a_gate = x @ W_gate^T`` and ``a_up = x @ W_up^T`` (two
+    dense GEMMs into the BF16 workspace buffers ``a_gate``, ``a_up``), ``a_act =
+    swiglu(a_gate, a_up)`` with the layer's ``swiglu_limit``, then ``shared_out = a_act @
+    W_down^T``; [fwd-new] ``forward_moe`` adds ``shared_out`` in the combine.  Stage rounding
+    as in ``prefill_forward``: fp32, then BF16 for the ``"bf16"`` variant (the pages' buffers
+    are BF16).  Returns each stage unrounded (``gate64`` ...) and rounded (``gate`` ...).
+    """
+    if variant not in VARIANTS:
+        raise ValueError(variant)
+    x = bf16_bits_to_f64(x_bits)
+    res: Dict[str, np.ndarray] = {}
+    res["gate64"] = x @ bf16_bits_to_f64(shared.gate).T
+    res["up64"] = x @ bf16_bits_to_f64(shared.up).T
+    res["gate"], res["up"] = _to_stage(res["gate64"], variant), _to_stage(res["up64"], variant)
+    res["act64"] = swiglu_clamp(res["gate"], res["up"], limit)
+    res["act"] = _to_stage(res["act64"], variant)
+    res["out64"] = res["act"] @ bf16_bits_to_f64(shared.down).T
+    res["out"] = _to_stage(res["out64"], variant)
+    return res
+
+
 class _Dequant:
     """Caches one projection's dequantised experts (built on first use)."""
 
@@ -343,7 +368,8 @@ def prefill_forward(case, variant: str = "bf16", logits: Optional[np.ndarray] = 
     has a router weight) -> top-k -> expert sort -> grouped gate/up GEMM with the A
     gather through ``sorted_token_ids`` -> clamped SwiGLU -> grouped down GEMM ->
     ``combine_indexed``.  Gate/up weights are one [2I, H] matrix per expert: rows
-    0..I-1 gate, rows I..2I-1 up (reading: concatenation).  No shared expert.
+    0..I-1 gate, rows I..2I-1 up (reading: concatenation).  When the case has a shared
+    expert, its BF16 output (``shared_expert_mlp``) joins the combine.
 
     ``logits`` overrides the case's routing input (routing bit-exactness is checked on
     shared logits).  Returns a dict: ``logits``, ``ids``, ``wts``, the four sort arrays,
@@ -368,7 +394,12 @@ def prefill_forward(case, variant: str = "bf16", logits: Optional[np.ndarray] = 
     res["act64"], res["act"] = act64, _to_stage(act64, variant)
     y64 = grouped_gemm(res["act"], srt["expert_offsets"], _Dequant(case.down, variant))
     res["Y64"], res["Y"] = y64, _to_stage(y64, variant)
-    out64 = combine_indexed(res["Y"], srt["token_to_perm"], wts)
+    shared_out = None
+    if getattr(case, "shared", None) is not None:
+        sh = shared_expert_mlp(case.x, case.shared, case.swiglu_limit, variant)
+        res["shared64"], res["shared"] = sh["out64"], sh["out"]
+        shared_out = sh["out"]
+    out64 = combine_indexed(res["Y"], srt["token_to_perm"], wts, shared_out)
     res["out64"] = out64
     return res
 
@@ -387,9 +418,12 @@ def token_forward(case, tokens: Sequence[int], ids: np.ndarray, wts: np.ndarray,
         dq["dn"] = _Dequant(case.down, variant)
     x = bf16_bits_to_f64(case.x)
     I = case.I
+    shared = None
+    if getattr(case, "shared", None) is not None:
+        shared = shared_expert_mlp(case.x[list(tokens)], case.shared, case.swiglu_limit, variant)["out"]
     outs, gs, ys = [], [], []
-    for t in tokens:
-        acc = np.zeros(case.H, dtype=np.float64)
+    for ti, t in enumerate(tokens):
+        acc = np.zeros(case.H, dtype=np.float64) if shared is None else shared[ti].copy()
         g_rows, y_rows = [], []
         for s in range(case.k):
             e = int(ids[t, s])

@@ -34,6 +34,8 @@ __all__ = [
     "GemmCase",
     "BlockCase",
     "ExpertWeights",
+    "SharedExpert",
+    "shared_expert_weights",
     "make_gemm_case",
     "make_block_case",
     "expert_weights",
@@ -51,6 +53,7 @@ _S_BIAS = 4
 _S_IDS = 5
 _S_SCALE2 = 6
 _S_ZIPF = 7
+_S_SHARED = 8  # + projection index 0 gate, 1 up, 2 down
 _S_W = 100  # + projection id
 PROJ_GEMM = 0
 PROJ_GATE_UP = 1
@@ -64,6 +67,8 @@ WORKLOADS: Dict[str, dict] = {
     "c0": dict(kind="gemm", T=64, E=16, k=8, N=256, K=512, seed=1000),
     # full routed-MoE block on one 256-row prefill chunk, with the router GEMM
     "c1": dict(kind="block", T=256, H=2048, I=768, E=64, k=8, routing="router", seed=1001),
+    # the same chunk with the shared expert (dense BF16 SwiGLU MLP, intermediate 768) in the combine
+    "c1s": dict(kind="block", T=256, H=2048, I=768, E=64, k=8, routing="router", seed=1001, shared_inter=768),
     # GLM-scale chunk, synthetic logits N(0,1) plus a per-expert bias N(0, 0.1^2)
     "c2": dict(kind="block", T=2048, H=5120, I=1536, E=160, k=8, routing="biased", seed=1002),
     # skewed routing: Zipf(1.2) popularity, 16 experts never chosen
@@ -174,6 +179,26 @@ def make_gemm_case(T: int = 64, E: int = 16, k: int = 8, N: int = 256, K: int = 
 
 
 @dataclasses.dataclass
+class SharedExpert:
+    """Dense BF16 SwiGLU MLP weights of the shared expert: gate and up [I, H], down [H, I]."""
+
+    I: int
+    gate: np.ndarray  # uint16 bf16 bits [I, H]
+    up: np.ndarray  # uint16 bf16 bits [I, H]
+    down: np.ndarray  # uint16 bf16 bits [H, I]
+
+
+def shared_expert_weights(seed: int, H: int, I: int) -> SharedExpert:
+    """BF16 N(0, 1/H) gate and up rows, so that with x ~ N(0, 1) the gate/up products are
+    ~N(0, 1) and the SwiGLU clamps act, and N(0, (0.025)^2/I) down rows, which puts the
+    shared output at the scale of the routed sum of the synthetic NVFP4 experts (std ~0.01)."""
+    def w(j, rows, cols, sd):
+        return bf16_bits_from_f32(_rng(seed, _S_SHARED, j).normal(0.0, sd, size=(rows, cols)).astype(np.float32))
+    return SharedExpert(I=I, gate=w(0, I, H, H ** -0.5), up=w(1, I, H, H ** -0.5),
+                        down=w(2, H, I, 0.025 * I ** -0.5))
+
+
+@dataclasses.dataclass
 class BlockCase:
     T: int
     H: int
@@ -188,6 +213,7 @@ class BlockCase:
     swiglu_limit: float = 7.0
     routed_scale: float = 1.0
     renormalize: int = 1
+    shared: Optional[SharedExpert] = None  # the shared expert, added in the combine
 
 
 def zipf_logits(seed: int, T: int, E: int, s: float = 1.2, n_zero: int = 16) -> np.ndarray:
@@ -219,7 +245,7 @@ def biased_logits(seed: int, T: int, E: int) -> np.ndarray:
 
 def make_block_case(T: int, H: int, I: int, E: int, k: int, routing: str, seed: int,
                     experts: Optional[List[int]] = None, absent: Tuple[int, ...] = (),
-                    with_weights: bool = True) -> BlockCase:
+                    with_weights: bool = True, shared_inter: Optional[int] = None) -> BlockCase:
     x = bf16_bits_from_f32(_rng(seed, _S_X, T).standard_normal((T, H), dtype=np.float32))
     router_w = None
     logits = None
@@ -239,8 +265,9 @@ def make_block_case(T: int, H: int, I: int, E: int, k: int, routing: str, seed: 
                            scale2=scale2_vector(seed, PROJ_GATE_UP, E))
         dn = ExpertWeights(N=H, K=I, packed=[None] * E, scales=[None] * E,
                            scale2=scale2_vector(seed, PROJ_DOWN, E))
+    shared = shared_expert_weights(seed, H, shared_inter) if shared_inter else None
     return BlockCase(T=T, H=H, I=I, E=E, k=k, x=x, router_w=router_w, logits=logits,
-                     gate_up=gu, down=dn)
+                     gate_up=gu, down=dn, shared=shared)
 
 
 def workload(name: str, T: Optional[int] = None, **kw):

@@ -351,3 +351,47 @@ def test_bf16_variant_gap_matches_pages_scale():
     gap = np.abs(outs["bf16"] - outs["exact"]).max() / np.abs(outs["exact"]).max()
     tab = _golden("grouped_gemm_error_table.json")["rows"]
     assert 3e-4 < gap < tab["grouped_vs_exact_fp32"][1]
+
+
+def test_shared_expert_diagonal_weights_closed_form():
+    """Diagonal weights turn the three GEMMs into elementwise scalings: with W_gate = a*Id,
+    W_up = b*Id, W_down = c*Id (exact in BF16) the MLP is out = c * swiglu(a*x, b*x).  a != b
+    and the clamp at L catch a transposed operand or swapped gate and up."""
+    H = 16
+    a, b, c = 3.0, -0.75, 0.5
+    eye = np.eye(H, dtype=np.float32)
+    sh = S.SharedExpert(I=H, gate=S.bf16_bits_from_f32(a * eye), up=S.bf16_bits_from_f32(b * eye),
+                        down=S.bf16_bits_from_f32(c * eye))
+    xs = np.linspace(-4.0, 4.0, 5 * H, dtype=np.float32).reshape(5, H)
+    xb = S.bf16_bits_from_f32(xs)
+    x = O.bf16_bits_to_f64(xb)
+    res = O.shared_expert_mlp(xb, sh, 7.0, "exact")
+    gate = np.minimum(a * x, 7.0)
+    expect = c * (gate / (1.0 + np.exp(-gate)) * np.clip(b * x, -7.0, 7.0))
+    np.testing.assert_allclose(res["out64"], expect, rtol=1e-6, atol=1e-7)  # fp32 stage roundings
+    assert (a * x > 7.0).any()  # the gate clamp is exercised
+    zero = O.shared_expert_mlp(np.zeros((2, H), np.uint16), sh, 7.0, "bf16")
+    assert (zero["out64"] == 0).all()
+
+
+def test_shared_expert_equals_single_routed_expert():
+    """The routed path with one expert, k = 1 (weight 1, identity sort) computes the same MLP
+    as the shared-expert oracle given that expert's dequantised BF16 weights: two code paths
+    (sort + grouped GEMM vs dense products) must agree to the last bit of the BF16 stages."""
+    c = S.make_block_case(T=7, H=64, I=32, E=1, k=1, routing="biased", seed=15)
+    res = O.prefill_forward(c, "bf16")
+    wgu = O.dequant_nvfp4(c.gate_up.packed[0], c.gate_up.scales[0], c.gate_up.scale2[0], "bf16")
+    wd = O.dequant_nvfp4(c.down.packed[0], c.down.scales[0], c.down.scale2[0], "bf16")
+    sh = S.SharedExpert(I=32, gate=S.bf16_bits_from_f32(wgu[:32]), up=S.bf16_bits_from_f32(wgu[32:]),
+                        down=S.bf16_bits_from_f32(wd))
+    dense = O.shared_expert_mlp(c.x, sh, c.swiglu_limit, "bf16")
+    np.testing.assert_array_equal(dense["out"], res["Y"])
+
+
+def test_shared_expert_joins_the_combine():
+    c = S.make_block_case(T=6, H=64, I=32, E=4, k=2, routing="biased", seed=16, shared_inter=32)
+    with_shared = O.prefill_forward(c, "bf16")
+    c.shared = None
+    without = O.prefill_forward(c, "bf16")
+    np.testing.assert_allclose(with_shared["out64"], without["out64"] + with_shared["shared"], rtol=1e-12,
+                               atol=1e-15)

@@ -33,6 +33,8 @@ WORKLOAD_DESC = {
     "c2": "GLM-scale routed MoE, 2048-row prefill chunk: hidden 5120, moe_intermediate 1536, 160 experts, top-8, "
           "synthetic logits N(0,1)+bias N(0,0.1)",
     "c3": "Zipf(1.2) skewed routing at GLM shapes, 8192 rows, 16 experts never chosen",
+    "c1s": "the 256-row chunk of c1 plus the shared expert (dense BF16 SwiGLU MLP, intermediate 768, cuBLAS "
+           "GEMMs) on a second stream, joined in the combine",
 }
 METRIC = "routed-MoE prefill tokens/s/layer"
 
@@ -200,10 +202,30 @@ def run_gpu(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     NEV = moe.MOE_FWD_NUM_EVENTS
+    sh = None
+    if case.shared is not None:  # shared expert on a second stream, joined before the combine
+        bits = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        sh = dict(gate=bits(case.shared.gate), up=bits(case.shared.up), down=bits(case.shared.down),
+                  out=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                  ws=torch.empty(moe.moe_shared_expert_workspace_bytes(T, H, case.shared.I), dtype=torch.uint8,
+                                 device=dev),
+                  side=torch.cuda.Stream(dev), fork=torch.cuda.Event(), ready=torch.cuda.Event())
 
     def step(events=None, st=None):
+        st = st if st is not None else stream
+        ready = None
+        if sh is not None:
+            sh["fork"].record(st)
+            sh["side"].wait_event(sh["fork"])
+            moe.moe_shared_expert_forward(x, sh["gate"], sh["up"], sh["down"], 7.0, ws=sh["ws"], out=sh["out"],
+                                          stream=sh["side"])
+            sh["ready"].record(sh["side"])
+            ready = sh["ready"]
         moe.moe_prefill_forward(cfg, x, gu.table, dn.table, ws, w_router=wr, logits=logits, out=out,
-                                stage_events=events, stream=st if st is not None else stream)
+                                stage_events=events, stream=st, shared_out=sh["out"] if sh else None,
+                                shared_ready=ready)
+        if sh is not None:
+            st.wait_stream(sh["side"])
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -333,9 +355,9 @@ def run_gpu(args):
                   "stage events, replayed one step at a time",
         "roofline": roof,
         "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
-        # router (when given router weights), top-k, sort histogram + scatter, gate/up GEMM with
-        # the fused SwiGLU, down GEMM, combine
-        "gpu_launches": (7 if wr is not None else 6) * args.steps,
+        # router (when given router weights), top-k, sort, gate/up GEMM with the fused SwiGLU,
+        # down GEMM, combine (+ the shared expert's SwiGLU; its GEMMs are cuBLAS kernels)
+        "gpu_launches": ((7 if wr is not None else 6) + (1 if sh is not None else 0)) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 4),
     }

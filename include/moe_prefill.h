@@ -239,6 +239,28 @@ int moe_swiglu_clamp(const uint16_t* gate, const uint16_t* up, int64_t rows, int
 int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const float* wts,
                         const uint16_t* shared_out, int T, int k, int H, uint16_t* out, void* stream);
 
+/* ---------------------------------------------------------------- shared expert */
+/*
+ * The shared expert over every row ("glm5next_mlp/forward.rs" (spark), forward_dense): a
+ * dense SwiGLU MLP with BF16 weights,
+ *   gate = x W_gate^T, up = x W_up^T (BF16 out), act = silu(min(gate, L)) * clamp(up, -L, L)
+ *   (BF16), shared_out = act W_down^T (BF16),
+ * FP32 accumulation.  Its output joins the routed sum in moe_prefill_forward's combine.
+ * The three products are plain dense GEMMs and run in cuBLAS; the SwiGLU is this library's.
+ *   x          device BF16 [T, H]
+ *   w_gate, w_up device BF16 [I, H];  w_down device BF16 [H, I]
+ *   ws, ws_bytes device workspace of at least moe_shared_expert_workspace_bytes(T, H, I) bytes,
+ *              256-byte aligned (it includes the cuBLAS workspace: nothing is allocated per call)
+ *   shared_out device BF16 [T, H] (output)
+ * Requirements: T >= 1, H and I multiples of 8, buffers 16-byte aligned, 0 < limit.
+ * The first call on a device creates its cuBLAS handle: make it before any stream capture that
+ * includes this call.  Calls from several host threads are serialised on the host.
+ */
+size_t moe_shared_expert_workspace_bytes(int T, int H, int I);
+int moe_shared_expert_forward(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
+                              const uint16_t* w_down, float limit, void* ws, size_t ws_bytes, uint16_t* shared_out,
+                              void* stream);
+
 /* ---------------------------------------------------------------- fused forward */
 typedef struct {
   int hidden;             /* H */
@@ -278,6 +300,11 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *              contents after the call: logits, ids, wts, the sort arrays, G, act, Y, at the
  *              offsets moe_workspace_layout reports.
  *   out        device BF16 [T, H]
+ *   shared_out device BF16 [T, H] or NULL: the shared expert's output, added in the combine
+ *              (moe_shared_expert_forward)
+ *   shared_ready NULL, or a cudaEvent_t (as void*) the stream waits for right before the
+ *              combine: shared_out may then be produced on another stream, concurrently with
+ *              the routed steps
  *   stage_events NULL, or a host array of MOE_FWD_NUM_EVENTS cudaEvent_t (as void*) recorded
  *              on `stream` before the first stage and after each of the 7 stages (router,
  *              top-k, sort count, sort scatter, gate/up GEMM, SwiGLU, down GEMM, combine
@@ -289,7 +316,7 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
 int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
                         const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,
                         const moe_expert_table* w_down, void* ws, size_t ws_bytes, uint16_t* out,
-                        void* const* stage_events, void* stream);
+                        const uint16_t* shared_out, void* shared_ready, void* const* stage_events, void* stream);
 
 /* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection). */
 typedef struct {

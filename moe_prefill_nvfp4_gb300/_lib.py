@@ -24,6 +24,7 @@ __all__ = [
     "moe_sort_by_expert_noalloc", "MOE_SORT_NOALLOC_MAX_INTS",
     "moe_w4a16_grouped_gemm", "moe_w4a16_grouped_gemm_swiglu", "MOE_FWD_SEPARATE_SWIGLU", "moe_dequant_nvfp4", "moe_swiglu_clamp", "moe_combine_indexed",
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
+    "moe_shared_expert_workspace_bytes", "moe_shared_expert_forward",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
 ]
 
@@ -86,8 +87,10 @@ _SIGS = {
     "moe_combine_indexed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_SZ, [ctypes.POINTER(MoePrefillConfig), _I]),
     "moe_workspace_layout": (_I, [ctypes.POINTER(MoePrefillConfig), _I, ctypes.POINTER(WorkspaceLayout)]),
-    "moe_prefill_forward": (_I, [ctypes.POINTER(MoePrefillConfig), _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P,
+    "moe_prefill_forward": (_I, [ctypes.POINTER(MoePrefillConfig), _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P,
                                  ctypes.POINTER(_P), _P]),
+    "moe_shared_expert_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _P, _F, _P, _SZ, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I)]),
 }
 
@@ -337,17 +340,43 @@ def moe_prefill_forward(cfg: MoePrefillConfig, x: torch.Tensor, w_gate_up: Exper
                         ws: torch.Tensor, w_router: Optional[torch.Tensor] = None,
                         logits: Optional[torch.Tensor] = None, router_bias: Optional[torch.Tensor] = None,
                         out: Optional[torch.Tensor] = None, stage_events: Optional[Sequence] = None,
-                        stream=None) -> torch.Tensor:
+                        stream=None, shared_out: Optional[torch.Tensor] = None, shared_ready=None) -> torch.Tensor:
+    """`shared_out`: the shared expert's BF16 [T, H] output, added in the combine; `shared_ready`:
+    a torch.cuda.Event the stream waits for before the combine (shared_out made on another stream)."""
     _need(x, torch.bfloat16, "x")
+    if shared_out is not None:
+        _need(shared_out, torch.bfloat16, "shared_out")
     T = x.shape[0]
     if out is None:
         out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=x.device)
     ev = None
     if stage_events is not None:
         ev = (_P * MOE_FWD_NUM_EVENTS)(*[e.cuda_event for e in stage_events])
+    ready = ctypes.c_void_p(shared_ready.cuda_event) if shared_ready is not None else None
     _check(lib().moe_prefill_forward(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router), _ptr(logits), _ptr(router_bias),
-                                     w_gate_up.handle, w_down.handle, _ptr(ws), ws.numel(), _ptr(out), ev,
-                                     _stream(stream)), "moe_prefill_forward")
+                                     w_gate_up.handle, w_down.handle, _ptr(ws), ws.numel(), _ptr(out),
+                                     _ptr(shared_out), ready, ev, _stream(stream)), "moe_prefill_forward")
+    return out
+
+
+def moe_shared_expert_workspace_bytes(T: int, H: int, I: int) -> int:
+    return int(lib().moe_shared_expert_workspace_bytes(T, H, I))
+
+
+def moe_shared_expert_forward(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                              limit: float = 7.0, ws: Optional[torch.Tensor] = None,
+                              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Shared expert (dense BF16 SwiGLU MLP): out = swiglu(x W_gate^T, x W_up^T) W_down^T."""
+    for t, n in ((x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _need(t, torch.bfloat16, n)
+    T, H = x.shape
+    I = w_gate.shape[0]
+    if ws is None:
+        ws = torch.empty(max(moe_shared_expert_workspace_bytes(T, H, I), 1), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_shared_expert_forward(_ptr(x), T, H, I, _ptr(w_gate), _ptr(w_up), _ptr(w_down), limit, _ptr(ws),
+                                           ws.numel(), _ptr(out), _stream(stream)), "moe_shared_expert_forward")
     return out
 
 

@@ -371,6 +371,28 @@ int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const f
   return combine_launch(Y, token_to_perm, wts, shared_out, T, k, H, out, as_stream(stream));
 }
 
+// ------------------------------------------------------------------------------------ shared expert
+
+size_t moe_shared_expert_workspace_bytes(int T, int H, int I) {
+  if (T < 1 || H < 8 || H % 8 != 0 || I < 8 || I % 8 != 0) return 0;
+  size_t a, b, c;
+  return shared_expert_ws_layout(T, I, &a, &b, &c);
+}
+
+int moe_shared_expert_forward(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
+                              const uint16_t* w_down, float limit, void* ws, size_t ws_bytes, uint16_t* shared_out,
+                              void* stream) {
+  if (!x || !w_gate || !w_up || !w_down || !ws || !shared_out || !(limit > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || H < 8 || H % 8 != 0 || I < 8 || I % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(shared_out) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_shared_expert_workspace_bytes(T, H, I)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  return shared_expert_launch(x, T, H, I, w_gate, w_up, w_down, limit, ws, shared_out, as_stream(stream));
+}
+
 // ------------------------------------------------------------------------------------------ forward
 
 static bool cfg_ok(const moe_prefill_config* c) {
@@ -415,17 +437,17 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows) {
 int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
                         const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,
                         const moe_expert_table* w_down, void* ws, size_t ws_bytes, uint16_t* out,
-                        void* const* stage_events, void* stream) {
+                        const uint16_t* shared_out, void* shared_ready, void* const* stage_events, void* stream) {
   if (!cfg_ok(cfg) || x == nullptr || out == nullptr || ws == nullptr || w_gate_up == nullptr || w_down == nullptr)
     return MOE_ERR_INVALID_ARG;
   if ((w_router == nullptr) == (logits_in == nullptr)) return MOE_ERR_INVALID_ARG;
   if (T < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int H = cfg->hidden, I = cfg->moe_intermediate, E = cfg->num_experts, k = cfg->top_k;
+  if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      (w_router && !aligned16(w_router)) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_INVALID_ARG;
   if (w_gate_up->E != E || w_gate_up->N != 2 * I || w_gate_up->K != H) return MOE_ERR_INVALID_ARG;
   if (w_down->E != E || w_down->N != H || w_down->K != I) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
-      (w_router && !aligned16(w_router)))
-    return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
   int rc = moe_workspace_layout(cfg, T, &L);
   if (rc != MOE_OK) return rc;
@@ -484,7 +506,9 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   ev(5);
   if ((rc = gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
   ev(6);
-  if ((rc = combine_launch(Y, t2p, wts, nullptr, T, k, H, out, st)) != MOE_OK) return rc;
+  if (shared_ready && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(shared_ready), 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((rc = combine_launch(Y, t2p, wts, shared_out, T, k, H, out, st)) != MOE_OK) return rc;
   ev(7);
   return MOE_OK;
 }

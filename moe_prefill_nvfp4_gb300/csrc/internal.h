@@ -53,6 +53,13 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// shared expert (shared_expert.cu): workspace = gate|up [T, 2I] BF16, act [T, I] BF16 and the
+// cuBLAS workspace, each 256-byte aligned; returns the total bytes
+constexpr size_t kSharedExpertBlasWorkspace = size_t(32) << 20;
+size_t shared_expert_ws_layout(int T, int I, size_t* off_gu, size_t* off_act, size_t* off_blas);
+int shared_expert_launch(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
+                         const uint16_t* w_down, float limit, void* ws, uint16_t* shared_out, cudaStream_t st);
+
 // SIMT kernels (small_kernels.cu)
 int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st);
 int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,

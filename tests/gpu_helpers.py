@@ -59,10 +59,31 @@ class DeviceBlock:
         self.layout = moe.moe_workspace_layout(self.cfg, case.T)
         self.ws = torch.empty(self.layout.total, dtype=torch.uint8, device="cuda")
         self.out = torch.empty(case.T, case.H, dtype=torch.bfloat16, device="cuda")
+        self.shared = None
+        if case.shared is not None:
+            sh = case.shared
+            self.shared = dict(gate=bf16_dev(sh.gate), up=bf16_dev(sh.up), down=bf16_dev(sh.down),
+                               out=torch.empty(case.T, case.H, dtype=torch.bfloat16, device="cuda"),
+                               ws=torch.empty(moe.moe_shared_expert_workspace_bytes(case.T, case.H, sh.I),
+                                              dtype=torch.uint8, device="cuda"))
 
-    def forward(self, stream=None):
+    def shared_forward(self, stream=None):
+        sh = self.shared
+        return moe.moe_shared_expert_forward(self.x, sh["gate"], sh["up"], sh["down"], self.case.swiglu_limit,
+                                             ws=sh["ws"], out=sh["out"], stream=stream)
+
+    def forward(self, stream=None, shared_ready=None):
+        """The routed forward; with a shared expert, its output (computed by shared_forward,
+        here on the same stream unless `shared_ready` says it comes from another) joins the
+        combine."""
+        shared_out = None
+        if self.shared is not None:
+            if shared_ready is None:
+                self.shared_forward(stream)
+            shared_out = self.shared["out"]
         return moe.moe_prefill_forward(self.cfg, self.x, self.gu.table, self.dn.table, self.ws, w_router=self.router_w,
-                                       logits=self.logits, out=self.out, stream=stream)
+                                       logits=self.logits, out=self.out, stream=stream, shared_out=shared_out,
+                                       shared_ready=shared_ready)
 
     def ws_view(self, name: str, dtype: torch.dtype, shape) -> torch.Tensor:
         off = getattr(self.layout, name)
@@ -84,6 +105,7 @@ class DeviceBlock:
             act=bf16_host(self.ws_view("act", torch.bfloat16, (R, c.I))),
             Y=bf16_host(self.ws_view("Y", torch.bfloat16, (R, c.H))),
             out=bf16_host(self.out),
+            shared=bf16_host(self.shared["out"]) if self.shared is not None else None,
         )
 
     def close(self):

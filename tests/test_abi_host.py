@@ -110,6 +110,28 @@ def test_forward_rejects(L):
                                 renormalize=1, routed_scale=1.0)
     f = L.moe_prefill_forward
     # neither router weight nor logits
-    assert f(ctypes.byref(cfg), P, 4, NULL, NULL, NULL, P, P, P, 1 << 30, P, NULL, NULL) == 1
+    assert f(ctypes.byref(cfg), P, 4, NULL, NULL, NULL, P, P, P, 1 << 30, P, NULL, NULL, NULL, NULL) == 1
     # both
-    assert f(ctypes.byref(cfg), P, 4, P, P, NULL, P, P, P, 1 << 30, P, NULL, NULL) == 1
+    assert f(ctypes.byref(cfg), P, 4, P, P, NULL, P, P, P, 1 << 30, P, NULL, NULL, NULL, NULL) == 1
+    # misaligned shared expert output
+    assert f(ctypes.byref(cfg), P, 4, P, NULL, NULL, P, P, ctypes.c_void_p(256), 1 << 30, P, ctypes.c_void_p(18), NULL,
+             NULL, NULL) == 1
+    # unknown flag bits
+    bad = _lib.MoePrefillConfig(hidden=2048, moe_intermediate=768, num_experts=64, top_k=8, swiglu_limit=7.0,
+                                renormalize=1, routed_scale=1.0, flags=4)
+    assert f(ctypes.byref(bad), P, 4, P, NULL, NULL, P, P, P, 1 << 30, P, NULL, NULL, NULL, NULL) == 1
+
+
+def test_shared_expert_rejects_and_sizes(L):
+    T, H, I = 4, 2048, 768
+    need = L.moe_shared_expert_workspace_bytes(T, H, I)
+    assert need >= (32 << 20) + T * 3 * I * 2  # gate|up, act and the cuBLAS workspace
+    assert L.moe_shared_expert_workspace_bytes(T, H, 12) == 0  # I % 8
+    f = L.moe_shared_expert_forward
+    W = ctypes.c_void_p(256)
+    assert f(NULL, T, H, I, P, P, P, 7.0, W, need, P, NULL) == 1
+    assert f(P, T, H, I, P, P, P, 0.0, W, need, P, NULL) == 1  # limit must be positive
+    assert f(P, T, H, 12, P, P, P, 7.0, W, need, P, NULL) == 2
+    assert f(P, 0, H, I, P, P, P, 7.0, W, need, P, NULL) == 2
+    assert f(P, T, H, I, P, P, P, 7.0, W, need - 1, P, NULL) == 3
+    assert f(P, T, H, I, P, P, P, 7.0, P, need, P, NULL) == 1  # workspace not 256-byte aligned

@@ -46,7 +46,7 @@ def _stagewise(case, st, R):
                     O.dequant_nvfp4(case.down.packed[e], case.down.scales[e], case.down.scale2[e], "bf16"))
     act = O.swiglu_clamp(st["G"][:R, :I], st["G"][:R, I:], case.swiglu_limit)
     Y = O.grouped_gemm(st["act"][:R], off, dn)
-    out = O.combine_indexed(st["Y"], st["token_to_perm"], st["wts"].astype(np.float64))
+    out = O.combine_indexed(st["Y"], st["token_to_perm"], st["wts"].astype(np.float64), st.get("shared"))
     return act, Y, out
 
 
@@ -76,6 +76,8 @@ def _check_full(case, separate=False):
         _, Y, out = _stagewise(case, dict(st, G=np.zeros((R, 2 * I))), R)
         errs = {"act": nerr(st["act"][:R], O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))}
     errs.update(Y=nerr(st["Y"][:R], Y), out=nerr(st["out"], out))
+    if case.shared is not None:
+        errs["shared"] = nerr(st["shared"], ref["shared64"])
     assert all(e < TOL_BF16 for e in errs.values()), ("bf16 stage-wise", errs)
     ex = chains["exact"]
     keys = ("G", "act", "Y", "out") if separate else ("act", "Y", "out")
@@ -215,4 +217,82 @@ def test_stage_events_inside_graph_capture():
         torch.cuda.synchronize()
         ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(evs) - 1)]
         assert all(m >= 0.0 for m in ms) and evs[0].elapsed_time(evs[-1]) > 0.0
+    db.close()
+
+
+# ---------------------------------------------------------------------------- shared expert
+
+
+def _shared_stagewise(case, T, clamped=False):
+    """Shared expert alone against the oracle: gate/up, act and out each on the GPU's own BF16
+    stage inputs (read back from the workspace), and the exact-FP32 chain."""
+    db = DeviceBlock(case)
+    out = db.shared_forward()
+    torch.cuda.synchronize()
+    I = case.shared.I
+    ws = db.shared["ws"]
+    gu = ws[:T * 2 * I * 2].view(torch.bfloat16).view(T, 2 * I)
+    a_off = (T * 2 * I * 2 + 255) // 256 * 256
+    act = ws[a_off:a_off + T * I * 2].view(torch.bfloat16).view(T, I)
+    gu_h, act_h, out_h = bf16_host(gu), bf16_host(act), bf16_host(out)
+    ref = O.shared_expert_mlp(case.x, case.shared, case.swiglu_limit, "bf16")
+    errs = dict(gate=nerr(gu_h[:, :I], ref["gate64"]), up=nerr(gu_h[:, I:], ref["up64"]),
+                act=nerr(act_h, O.swiglu_clamp(gu_h[:, :I], gu_h[:, I:], case.swiglu_limit)),
+                out=nerr(out_h, act_h @ O.bf16_bits_to_f64(case.shared.down).T))
+    assert all(e < TOL_BF16 for e in errs.values()), errs
+    ex = O.shared_expert_mlp(case.x, case.shared, case.swiglu_limit, "exact")
+    assert nerr(out_h, ex["out64"]) < TOL_EXACT, ("exact chain", nerr(out_h, ex["out64"]))
+    if clamped:  # both clamps are exercised
+        assert (ref["gate64"] > case.swiglu_limit).any() and (np.abs(ref["up64"]) > case.swiglu_limit).any()
+    db.close()
+
+
+@pytest.mark.parametrize("T,H,I,gain", [(37, 512, 256, 4.0), (256, 2048, 768, 1.0)],
+                         ids=["ragged-small-clamped", "c1-size"])
+def test_shared_expert_vs_oracle(T, H, I, gain):
+    """`gain` scales the gate and up weights (a power of two: exact in BF16) so that |g| and |u|
+    pass the SwiGLU limit and both clamps act."""
+    c = S.make_block_case(T=T, H=H, I=I, E=2, k=1, routing="biased", seed=36, shared_inter=I)
+    scale = lambda w: S.bf16_bits_from_f32((O.bf16_bits_to_f64(w) * gain).astype(np.float32))
+    c.shared = S.SharedExpert(I=I, gate=scale(c.shared.gate), up=scale(c.shared.up), down=c.shared.down)
+    _shared_stagewise(c, T, clamped=gain > 1.0)
+
+
+def test_c1_chunk_with_shared_expert():
+    """The 256-row chunk with the shared expert in the combine (routed steps stage by stage,
+    the shared output against the oracle, the exact chain)."""
+    _check_full(S.workload("c1s"))
+
+
+def test_shared_expert_on_a_second_stream():
+    """The shared expert on its own stream, joined by an event before the combine: the same
+    bits as the serial forward, eagerly and from a captured graph."""
+    c = S.make_block_case(T=96, H=512, I=256, E=12, k=4, routing="biased", seed=37, shared_inter=256)
+    db = DeviceBlock(c)
+    db.forward()
+    torch.cuda.synchronize()
+    serial = db.out.clone()
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ready, fork = torch.cuda.Event(), torch.cuda.Event()
+
+    def run():
+        fork.record(main)
+        side.wait_event(fork)
+        db.shared_forward(stream=side)
+        ready.record(side)
+        db.forward(stream=main, shared_ready=ready)
+        main.wait_stream(side)
+
+    db.out.zero_()
+    with torch.cuda.stream(main):
+        run()
+    torch.cuda.synchronize()
+    assert torch.equal(db.out.view(torch.int16), serial.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        run()
+    db.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(db.out.view(torch.int16), serial.view(torch.int16))
     db.close()

@@ -53,6 +53,7 @@ typedef enum {
 #define MOE_DEVERR_TIMEOUT 3         /* a pipeline wait in a GEMM kernel exceeded its limit  */
 #define MOE_DEVERR_NAN_LOGIT 4       /* a NaN routing logit; it is ranked below every number */
 #define MOE_DEVERR_BAD_GATHER 5      /* a gather index outside [0, a_rows); row 0 was read */
+#define MOE_DEVERR_SMALL_ROWS 6      /* an expert has more rows than the small-row products take */
 
 /* output element type of the grouped GEMM */
 #define MOE_DTYPE_BF16 0
@@ -239,6 +240,28 @@ int moe_swiglu_clamp(const uint16_t* gate, const uint16_t* up, int64_t rows, int
 int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const float* wts,
                         const uint16_t* shared_out, int T, int k, int H, uint16_t* out, void* stream);
 
+/* ---------------------------------------------------------------- small-row products */
+/*
+ * The grouped W4A16 products for chunks with at most 8 rows per expert (decode-like): the same
+ * C[p, n] = sum_k A[g(p), k] * W_e[n, k] as moe_w4a16_grouped_gemm, computed without tensor
+ * cores with the dequantised weights kept in FP32 (E2M1 * E4M3 exact, scale2 applied to the
+ * FP32 sums), the arithmetic of the pages' decode GEMV ("Module forward_prefill_gemm",
+ * "What is NOT bit-identical", item 2); C is BF16.  _swiglu: a gate/up table of N = 2I rows
+ * gives act[p, j] = silu(min(g, L)) * clamp(u, -L, L) from the FP32 gate and up sums.
+ * Arguments as moe_w4a16_grouped_gemm(_swiglu) (C BF16 only).  An expert with more than 8 rows
+ * sets MOE_DEVERR_SMALL_ROWS and its rows are not written; expert_offsets outside [0, R] set
+ * MOE_DEVERR_BAD_OFFSETS.  Requires lda % 8 == 0 and A 16-byte aligned.
+ * Measured on GB300 at GLM shapes (hidden 5120, intermediate 1536, 160 experts, top-8), whole
+ * forward: 0.155 / 0.204 / 0.287 / 0.462 ms at T = 1 / 2 / 4 / 8 rows against 0.116 / 0.173 /
+ * 0.233 / 0.379 ms with the tensor-core GEMMs: the numerics option, not the fast path.
+ */
+int moe_w4a16_grouped_gemv(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                           const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* C, int ldc,
+                           void* stream);
+int moe_w4a16_grouped_gemv_swiglu(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                  const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* act,
+                                  int ld_act, float limit, void* stream);
+
 /* ---------------------------------------------------------------- shared expert */
 /*
  * The shared expert over every row ("glm5next_mlp/forward.rs" (spark), forward_dense): a
@@ -276,6 +299,10 @@ typedef struct {
 /* moe_prefill_config.flags: run the SwiGLU as its own kernel on a materialised G [R, 2I]
  * (BF16) instead of in the gate/up GEMM's epilogue (the default); for inspection and tests. */
 #define MOE_FWD_SEPARATE_SWIGLU 1
+/* moe_prefill_config.flags: chunks of at most 8 rows take the small-row products
+ * (moe_w4a16_grouped_gemv*: FP32 dequantised weights, the numerics of the pages' decode GEMV)
+ * instead of the tensor-core GEMMs (faster on this GPU: see the small-row products' header). */
+#define MOE_FWD_SMALL_ROWS 2
 
 /* Workspace bytes for moe_prefill_forward with up to max_rows rows (0 on a bad config). */
 size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
@@ -311,7 +338,9 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *              -> events 0..7 bracket them; a skipped router records event 1 = event 0, and
  *              with the fused SwiGLU (the default) event 5 = event 4).
  * The SwiGLU runs in the gate/up GEMM's epilogue (moe_w4a16_grouped_gemm_swiglu) unless
- * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.
+ * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.  With
+ * MOE_FWD_SMALL_ROWS, chunks of T <= 8 rows take the small-row products (FP32 dequantised
+ * weights, as the pages' decode GEMV) instead of the tensor-core GEMMs.
  */
 int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T, const uint16_t* w_router,
                         const float* logits_in, const float* router_bias, const moe_expert_table* w_gate_up,

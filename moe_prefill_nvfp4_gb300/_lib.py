@@ -22,7 +22,8 @@ __all__ = [
     "MoePrefillConfig", "WorkspaceLayout", "ExpertTable",
     "moe_router_logits", "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
     "moe_sort_by_expert_noalloc", "MOE_SORT_NOALLOC_MAX_INTS",
-    "moe_w4a16_grouped_gemm", "moe_w4a16_grouped_gemm_swiglu", "MOE_FWD_SEPARATE_SWIGLU", "moe_dequant_nvfp4", "moe_swiglu_clamp", "moe_combine_indexed",
+    "moe_w4a16_grouped_gemm", "moe_w4a16_grouped_gemm_swiglu", "MOE_FWD_SEPARATE_SWIGLU", "moe_dequant_nvfp4",
+    "moe_w4a16_grouped_gemv", "moe_w4a16_grouped_gemv_swiglu", "MOE_FWD_SMALL_ROWS", "moe_swiglu_clamp", "moe_combine_indexed",
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
     "moe_shared_expert_workspace_bytes", "moe_shared_expert_forward",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
@@ -35,11 +36,12 @@ MOE_DTYPE_BF16 = 0
 MOE_DTYPE_F32 = 1
 MOE_FWD_NUM_EVENTS = 8
 MOE_FWD_SEPARATE_SWIGLU = 1  # moe_prefill_config.flags: SwiGLU as its own kernel on a materialised G
+MOE_FWD_SMALL_ROWS = 2  # moe_prefill_config.flags: small-row products (FP32 weights) for chunks of <= 8 rows
 MOE_SORT_NOALLOC_MAX_INTS = 65536  # int32 entries of the library's fixed sort scratch
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_NOT_BUILT_FOR_DEVICE", 7: "MOE_ERR_SCRATCH_LIMIT"}
 DEVERR = {0: "none", 1: "bad expert id", 2: "bad expert offsets", 3: "pipeline wait timeout", 4: "NaN logit",
-          5: "bad gather index"}
+          5: "bad gather index", 6: "more than 8 rows for the small-row products"}
 
 
 class MoeError(RuntimeError):
@@ -82,6 +84,8 @@ _SIGS = {
     "moe_sort_by_expert_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_w4a16_grouped_gemm": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _I, _P]),
     "moe_w4a16_grouped_gemm_swiglu": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _F, _P]),
+    "moe_w4a16_grouped_gemv": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _P]),
+    "moe_w4a16_grouped_gemv_swiglu": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _F, _P]),
     "moe_dequant_nvfp4": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "moe_swiglu_clamp": (_I, [_P, _P, _I64, _I64, _I64, _P, _I64, _F, _P]),
     "moe_combine_indexed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -267,6 +271,38 @@ def moe_w4a16_grouped_gemm_swiglu(A: torch.Tensor, W: ExpertTable, expert_offset
                                                _ptr(expert_offsets), R, _ptr(out), out.stride(0), limit,
                                                _stream(stream)),
            "moe_w4a16_grouped_gemm_swiglu")
+    return out
+
+
+def moe_w4a16_grouped_gemv(A: torch.Tensor, W: ExpertTable, expert_offsets: torch.Tensor, R: int,
+                           gather_ids: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None, stream=None):
+    """Small-row product (<= 8 rows per expert), FP32 dequantised weights, BF16 [R, N]."""
+    _need(A, torch.bfloat16, "A")
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    if gather_ids is not None:
+        _need(gather_ids, torch.int32, "gather_ids")
+    if out is None:
+        out = torch.empty(R, W.N, dtype=torch.bfloat16, device=A.device)
+    _check(lib().moe_w4a16_grouped_gemv(_ptr(A), A.shape[0], A.stride(0), _ptr(gather_ids), W.handle,
+                                        _ptr(expert_offsets), R, _ptr(out), out.stride(0), _stream(stream)),
+           "moe_w4a16_grouped_gemv")
+    return out
+
+
+def moe_w4a16_grouped_gemv_swiglu(A: torch.Tensor, W: ExpertTable, expert_offsets: torch.Tensor, R: int,
+                                  limit: float = 7.0, gather_ids: Optional[torch.Tensor] = None,
+                                  out: Optional[torch.Tensor] = None, stream=None):
+    """Small-row gate/up product with the clamped SwiGLU: BF16 act [R, I]."""
+    _need(A, torch.bfloat16, "A")
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    if gather_ids is not None:
+        _need(gather_ids, torch.int32, "gather_ids")
+    if out is None:
+        out = torch.empty(R, W.N // 2, dtype=torch.bfloat16, device=A.device)
+    _check(lib().moe_w4a16_grouped_gemv_swiglu(_ptr(A), A.shape[0], A.stride(0), _ptr(gather_ids), W.handle,
+                                               _ptr(expert_offsets), R, _ptr(out), out.stride(0), limit,
+                                               _stream(stream)),
+           "moe_w4a16_grouped_gemv_swiglu")
     return out
 
 

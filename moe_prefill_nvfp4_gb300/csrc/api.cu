@@ -18,6 +18,7 @@ struct moe_expert_table {
   int device;
   CUtensorMap* d_maps;    // [E][2]
   const void** d_packed;  // [E]
+  const void** d_scales;  // [E]
   float* d_scale2;        // [E]
 };
 
@@ -171,12 +172,15 @@ int moe_expert_table_create(const void* const* packed, const void* const* scales
   t->device = current_device();
   t->d_maps = nullptr;
   t->d_packed = nullptr;
+  t->d_scales = nullptr;
   t->d_scale2 = nullptr;
   bool ok = cudaMalloc(&t->d_maps, maps.size() * sizeof(CUtensorMap)) == cudaSuccess &&
             cudaMalloc(&t->d_packed, (size_t)E * sizeof(void*)) == cudaSuccess &&
+            cudaMalloc(&t->d_scales, (size_t)E * sizeof(void*)) == cudaSuccess &&
             cudaMalloc(&t->d_scale2, (size_t)E * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_packed, packed, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(t->d_scales, scales, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_scale2, scale2, (size_t)E * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
   if (!ok) {
     moe_expert_table_destroy(t);
@@ -191,6 +195,7 @@ int moe_expert_table_destroy(moe_expert_table* t) {
   cudaDeviceSynchronize();
   cudaFree(t->d_maps);
   cudaFree(t->d_packed);
+  cudaFree(t->d_scales);
   cudaFree(t->d_scale2);
   delete t;
   return MOE_OK;
@@ -336,6 +341,52 @@ int moe_w4a16_grouped_gemm_swiglu(const uint16_t* A, int a_rows, int lda, const 
                       W->N / 2, limit);
 }
 
+static int gemv_checked(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids, const moe_expert_table* W,
+                        const int32_t* expert_offsets, int R, uint16_t* C, int ldc, int swiglu_half, float limit,
+                        cudaStream_t st) {
+  if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
+  if (swiglu_half && (W->N != 2 * swiglu_half || !(limit > 0.f))) return MOE_ERR_INVALID_ARG;
+  const int out_cols = swiglu_half ? swiglu_half : W->N;
+  if (a_rows < 1 || R < 1 || lda < W->K || lda % 8 != 0 || ldc < out_cols) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A)) return MOE_ERR_INVALID_ARG;
+  int rc = ensure_device();
+  if (rc != MOE_OK) return rc;
+  if (current_device() != W->device) return MOE_ERR_INVALID_ARG;
+  SmallRowsArgs a;
+  a.A = A;
+  a.lda = lda;
+  a.a_rows = a_rows;
+  a.gather = gather_ids;
+  a.packed = W->d_packed;
+  a.scales = W->d_scales;
+  a.scale2 = W->d_scale2;
+  a.offsets = expert_offsets;
+  a.E = W->E;
+  a.N = W->N;
+  a.K = W->K;
+  a.R = R;
+  a.swiglu_half = swiglu_half;
+  a.limit = limit;
+  a.C = C;
+  a.ldc = ldc;
+  a.err = device_error_word();
+  return small_rows_launch(a, st);
+}
+
+int moe_w4a16_grouped_gemv(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                           const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* C, int ldc,
+                           void* stream) {
+  return gemv_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, C, ldc, 0, 0.f, as_stream(stream));
+}
+
+int moe_w4a16_grouped_gemv_swiglu(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                  const moe_expert_table* W, const int32_t* expert_offsets, int R, uint16_t* act,
+                                  int ld_act, float limit, void* stream) {
+  if (W == nullptr) return MOE_ERR_INVALID_ARG;
+  return gemv_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, act, ld_act, W->N / 2, limit,
+                      as_stream(stream));
+}
+
 int moe_dequant_nvfp4(const void* packed, const void* scales, float scale2, int N, int K, uint16_t* out,
                       void* stream) {
   if (packed == nullptr || scales == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
@@ -398,7 +449,8 @@ int moe_shared_expert_forward(const uint16_t* x, int T, int H, int I, const uint
 static bool cfg_ok(const moe_prefill_config* c) {
   return c != nullptr && c->hidden >= 256 && c->hidden % 256 == 0 && c->moe_intermediate >= 256 &&
          c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 512 && c->top_k >= 1 &&
-         c->top_k <= 32 && c->top_k <= c->num_experts && (c->flags & ~MOE_FWD_SEPARATE_SWIGLU) == 0;
+         c->top_k <= 32 && c->top_k <= c->num_experts &&
+         (c->flags & ~(MOE_FWD_SEPARATE_SWIGLU | MOE_FWD_SMALL_ROWS)) == 0;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -494,7 +546,13 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   ev(2);
   if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st)) != MOE_OK) return rc;
   ev(3);
-  if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
+  // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
+  const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
+  if (small) {
+    rc = gemv_checked(x, T, H, sti, w_gate_up, off, R, act, I, I, cfg->swiglu_limit, st);
+    if (rc != MOE_OK) return rc;
+    ev(4);
+  } else if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
     if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
@@ -504,7 +562,9 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     ev(4);
   }
   ev(5);
-  if ((rc = gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+  rc = small ? gemv_checked(act, R, I, nullptr, w_down, off, R, Y, H, 0, 0.f, st)
+             : gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st);
+  if (rc != MOE_OK) return rc;
   ev(6);
   if (shared_ready && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(shared_ready), 0) != cudaSuccess)
     return MOE_ERR_CUDA;

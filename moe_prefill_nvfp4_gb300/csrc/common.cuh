@@ -304,6 +304,15 @@ MOE_DEV uint32_t dequant_pair(uint32_t lut2, uint32_t scale_h, float s2) {
   return out;
 }
 
+// f16 pair (two E2M1 values) times one f16 (the block scale, low half of scale_h): two exact
+// FP32 products (mixed-precision FMA with a -0 addend, as in dequant_pair).
+MOE_DEV void f16x2_times_f16(uint32_t lut2, uint32_t scale_h, float& lo, float& hi) {
+  asm("{\n .reg .b16 l, h, a, unused;\n mov.b32 {l, h}, %2;\n mov.b32 {a, unused}, %3;\n"
+      " fma.rn.f32.f16 %0, l, a, 0f80000000;\n fma.rn.f32.f16 %1, h, a, 0f80000000;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(lut2), "r"(scale_h));
+}
+
 MOE_DEV void dequant64(const uint32_t (&w)[8], uint32_t sc, float s2, uint32_t (&out)[32]) {
   uint32_t a01, a23;
   e4m3x4_to_f16x2(sc, a01, a23);

@@ -53,6 +53,24 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// small-row products (small_rows.cu): at most 8 rows per expert, FP32 weights, BF16 out
+struct SmallRowsArgs {
+  const uint16_t* A;
+  int lda, a_rows;
+  const int32_t* gather;      // [R] or NULL (identity)
+  const void* const* packed;  // device [E]
+  const void* const* scales;  // device [E]
+  const float* scale2;        // device [E]
+  const int32_t* offsets;     // [E+1]
+  int E, N, K, R;
+  int swiglu_half;            // 0: C = A W^T [R, N]; I: gate/up pair -> SwiGLU act [R, I]
+  float limit;
+  uint16_t* C;
+  int ldc;
+  int* err;
+};
+int small_rows_launch(const SmallRowsArgs& a, cudaStream_t st);
+
 // shared expert (shared_expert.cu): workspace = gate|up [T, 2I] BF16, act [T, I] BF16 and the
 // cuBLAS workspace, each 256-byte aligned; returns the total bytes
 constexpr size_t kSharedExpertBlasWorkspace = size_t(32) << 20;

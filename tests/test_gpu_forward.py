@@ -38,16 +38,23 @@ def _no_device_error():
     assert moe.moe_get_device_error() == 0
 
 
-def _stagewise(case, st, R):
-    """Oracle of each float stage on the GPU's own BF16 stage inputs (BF16-rounding variant)."""
+def _stagewise(case, st, R, wvar="bf16"):
+    """Oracle of each float stage on the GPU's own BF16 stage inputs, with the weights the GPU
+    path multiplies with (BF16-rounded, or FP32 for the small-row products)."""
     I = case.I
     off = st["expert_offsets"]
     dn = lambda e: (None if case.down.packed[e] is None else
-                    O.dequant_nvfp4(case.down.packed[e], case.down.scales[e], case.down.scale2[e], "bf16"))
+                    O.dequant_nvfp4(case.down.packed[e], case.down.scales[e], case.down.scale2[e], wvar))
     act = O.swiglu_clamp(st["G"][:R, :I], st["G"][:R, I:], case.swiglu_limit)
     Y = O.grouped_gemm(st["act"][:R], off, dn)
     out = O.combine_indexed(st["Y"], st["token_to_perm"], st["wts"].astype(np.float64), st.get("shared"))
     return act, Y, out
+
+
+def _small_rows(case, separate=False, flags=0) -> bool:
+    """With MOE_FWD_SMALL_ROWS, chunks of <= 8 rows take the small-row products (FP32
+    dequantised weights, as the pages' decode GEMV): their reference is the exact-weight oracle."""
+    return case.T <= 8 and not separate and bool(flags & moe.MOE_FWD_SMALL_ROWS)
 
 
 def _check_full(case, separate=False):
@@ -62,18 +69,19 @@ def _check_full(case, separate=False):
     if case.router_w is not None:
         assert nerr(st["logits"], O.router_logits(case.x, case.router_w)) < 1e-5
     chains = {v: O.prefill_forward(case, v, logits=shared_logits) for v in ("bf16", "exact")}
-    ref = chains["bf16"]
+    wvar = "exact" if _small_rows(case, separate) else "bf16"  # the weights the GPU path multiplies with
+    ref = chains[wvar]
     for key in ("ids", "sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm"):
         np.testing.assert_array_equal(st[key], ref[key], err_msg=key)
     np.testing.assert_allclose(st["wts"], ref["wts"], rtol=2e-6, atol=1e-7)
     R = int(ref["expert_offsets"][-1])
     I = case.I
     if separate:
-        act, Y, out = _stagewise(case, st, R)
+        act, Y, out = _stagewise(case, st, R, wvar)
         errs = {"G": nerr(st["G"][:R], ref["G64"][:R]), "act": nerr(st["act"][:R], act)}
     else:
         G = ref["G64"][:R]
-        _, Y, out = _stagewise(case, dict(st, G=np.zeros((R, 2 * I))), R)
+        _, Y, out = _stagewise(case, dict(st, G=np.zeros((R, 2 * I))), R, wvar)
         errs = {"act": nerr(st["act"][:R], O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))}
     errs.update(Y=nerr(st["Y"][:R], Y), out=nerr(st["out"], out))
     if case.shared is not None:
@@ -102,6 +110,30 @@ def test_single_row():
 def test_absent_expert_block(separate):
     c = S.make_block_case(T=64, H=256, I=256, E=6, k=2, routing="biased", seed=33, absent=(2,))
     _check_full(c, separate)
+
+
+@pytest.mark.parametrize("flags", [0, 2], ids=["tensor-core-gemms", "small-row-products"])
+def test_eight_row_chunk(flags):
+    """T = 8 at GLM-like widths: the default tensor-core GEMMs, and the small-row products that
+    MOE_FWD_SMALL_ROWS selects."""
+    c = S.make_block_case(T=8, H=1024, I=512, E=40, k=8, routing="biased", seed=38)
+    db = DeviceBlock(c)
+    db.cfg.flags = flags
+    db.forward()
+    torch.cuda.synchronize()
+    st = db.stages()
+    db.close()
+    wvar = "exact" if flags else "bf16"
+    ref = O.prefill_forward(c, wvar, logits=c.logits)
+    for key in ("ids", "sorted_token_ids", "expert_offsets", "token_to_perm"):
+        np.testing.assert_array_equal(st[key], ref[key], err_msg=key)
+    R = c.T * c.k
+    G = ref["G64"]
+    _, Y, out = _stagewise(c, dict(st, G=np.zeros((R, 2 * c.I))), R, wvar)
+    errs = dict(act=nerr(st["act"], O.swiglu_clamp(G[:, :c.I], G[:, c.I:], c.swiglu_limit)), Y=nerr(st["Y"], Y),
+                out=nerr(st["out"], out))
+    assert all(e < TOL_BF16 for e in errs.values()), errs
+    assert nerr(st["out"], O.prefill_forward(c, "exact", logits=c.logits)["out64"]) < TOL_EXACT
 
 
 @pytest.mark.parametrize("separate", [False, True], ids=["fused-swiglu", "separate-swiglu"])
@@ -144,10 +176,11 @@ def _check_sampled(case, tokens, variants=("bf16",)):
     rows = torch.from_numpy(t2p[tokens].reshape(-1)).long().cuda()
     Y = bf16_host(Yd[rows])
     A = bf16_host(Ad[rows])
-    # bf16 variant: act against the SwiGLU of the oracle's unrounded G (the fused epilogue never
-    # rounds G), then Y and out stage by stage on the GPU's own stage inputs
+    # act against the SwiGLU of the oracle's unrounded G (the fused epilogue never rounds G),
+    # then Y and out stage by stage on the GPU's own stage inputs; weights as the GPU path uses
+    # them (BF16-rounded; FP32 for the small-row products)
     dq = {}
-    ref = O.token_forward(case, tokens, rid, rw, "bf16", dq)
+    ref = O.token_forward(case, tokens, rid, rw, "exact" if _small_rows(case) else "bf16", dq)
     G64 = ref["G64"].reshape(-1, 2 * I)
     ea = nerr(A, O.swiglu_clamp(G64[:, :I], G64[:, I:], case.swiglu_limit))
     ys = np.stack([A[r] @ dq["dn"](int(e)).astype(np.float64).T for r, e in enumerate(rid[tokens].reshape(-1))])

@@ -298,3 +298,67 @@ def test_gemm_swiglu_fused(T, E, k, I, big, identity):
     # difference of g and u carried through the SwiGLU
     assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-4 * np.abs(ref).max()).all()
     proj.close()
+
+
+# ---------------------------------------------------------------------------- small-row products
+
+
+def _small_case(T, E, k, N, K, seed, absent=()):
+    c = S.make_gemm_case(T=T, E=E, k=k, N=N, K=K, seed=seed, absent=absent)
+    srt = moe.moe_sort_by_expert(torch.from_numpy(c.ids).cuda(), c.E)
+    return c, srt, upload(c.w)
+
+
+@pytest.mark.parametrize("T,E,k,N,K,identity", [(8, 16, 8, 256, 512, False), (5, 40, 6, 384, 1024, True),
+                                                (1, 8, 8, 264, 256, False)],
+                         ids=["8-rows", "5-rows-identity", "1-row-ragged-N"])
+def test_gemv_vs_exact_oracle(T, E, k, N, K, identity):
+    """The small-row product keeps the dequantised weights in FP32 (the pages' decode GEMV), so
+    its reference is the exact variant; the only rounding left is C's BF16 rounding."""
+    c, srt, proj = _small_case(T, E, k, N, K, seed=51 + T, absent=(3,))
+    R = T * k
+    if identity:
+        A = bf16_dev(c.x)[srt["sorted_token_ids"].long()].contiguous()
+        C = moe.moe_w4a16_grouped_gemv(A, proj.table, srt["expert_offsets"], R)
+    else:
+        C = moe.moe_w4a16_grouped_gemv(bf16_dev(c.x), proj.table, srt["expert_offsets"], R,
+                                       gather_ids=srt["sorted_token_ids"])
+    torch.cuda.synchronize()
+    s = {kk: v.cpu().numpy() for kk, v in srt.items()}
+    ref = _oracle_gemm(c, s, "exact")
+    got = bf16_host(C)
+    o = s["expert_offsets"]
+    assert (got[o[3]:o[4]] == 0).all()  # absent expert
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()).all()
+    assert nerr(got, _oracle_gemm(c, s, "bf16")) < TOL_BF16  # and close to the BF16-weight variant
+    proj.close()
+
+
+def test_gemv_swiglu_vs_exact_oracle():
+    T, E, k, I, K = 8, 12, 8, 256, 512
+    c, srt, proj = _small_case(T, E, k, 2 * I, K, seed=57)
+    c.w.scale2[:] = c.w.scale2 * 200.0  # |g|, |u| past the limit: both clamps act
+    proj.close()
+    proj = upload(c.w)
+    act = moe.moe_w4a16_grouped_gemv_swiglu(bf16_dev(c.x), proj.table, srt["expert_offsets"], T * k, limit=7.0,
+                                            gather_ids=srt["sorted_token_ids"])
+    torch.cuda.synchronize()
+    s = {kk: v.cpu().numpy() for kk, v in srt.items()}
+    G = _oracle_gemm(c, s, "exact")
+    ref = O.swiglu_clamp(G[:, :I], G[:, I:], 7.0)
+    assert (np.abs(G[:, :I]) > 7.0).mean() > 0.05 and (np.abs(G[:, I:]) > 7.0).mean() > 0.05
+    got = bf16_host(act)
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-4 * np.abs(ref).max()).all()
+    proj.close()
+
+
+def test_gemv_refuses_more_than_8_rows_per_expert():
+    c, srt, proj = _small_case(16, 4, 2, 128, 256, seed=58)  # 32 slots on 4 experts
+    out = torch.full((32, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    moe.moe_w4a16_grouped_gemv(bf16_dev(c.x), proj.table, srt["expert_offsets"], 32,
+                               gather_ids=srt["sorted_token_ids"], out=out)
+    assert moe.moe_get_device_error() == 6
+    off = srt["expert_offsets"].cpu().numpy()
+    big = [e for e in range(4) if off[e + 1] - off[e] > 8]
+    assert big and all((out[off[e]:off[e + 1]] == 3.0).all() for e in big)  # not written
+    proj.close()

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -30,10 +31,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Filled once per device under g_mu; g_arch_ok is published last (release) and read first
+// (acquire), so a thread that sees 1 also sees the error word and the SM count.
 int* g_err_addr[kMaxDevices] = {nullptr};
 int g_sm_count[kMaxDevices] = {0};
-int g_arch_ok[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 not sm_103
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int> g_arch_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 not sm_103
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 int current_device() {
   int d = -1;
@@ -45,22 +48,22 @@ int current_device() {
 int ensure_device() {
   const int d = current_device();
   if (d < 0) return MOE_ERR_CUDA;
-  if (g_arch_ok[d] == 1) return MOE_OK;
+  if (g_arch_ok[d].load(std::memory_order_acquire) == 1) return MOE_OK;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_arch_ok[d] == 0) {
+  if (g_arch_ok[d].load(std::memory_order_relaxed) == 0) {
     cudaDeviceProp p;
     if (cudaGetDeviceProperties(&p, d) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(p.major == 10 && p.minor == 3)) {
-      g_arch_ok[d] = -1;
+      g_arch_ok[d].store(-1, std::memory_order_release);
     } else {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return MOE_ERR_CUDA;
       g_err_addr[d] = static_cast<int*>(addr);
       g_sm_count[d] = p.multiProcessorCount;
-      g_arch_ok[d] = 1;
+      g_arch_ok[d].store(1, std::memory_order_release);
     }
   }
-  return g_arch_ok[d] == 1 ? MOE_OK : MOE_ERR_NOT_BUILT_FOR_DEVICE;
+  return g_arch_ok[d].load(std::memory_order_relaxed) == 1 ? MOE_OK : MOE_ERR_NOT_BUILT_FOR_DEVICE;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -82,19 +85,22 @@ int* device_error_word() {
 int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const cuuint64_t* dims,
                 const cuuint64_t* strides_bytes, const cuuint32_t* box, const cuuint32_t* elem_strides,
                 CUtensorMapSwizzle swizzle) {
-  if (g_encode == nullptr) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = g_encode.load(std::memory_order_acquire);
+  if (encode == nullptr) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_encode == nullptr) {
+    encode = g_encode.load(std::memory_order_relaxed);
+    if (encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
       if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
               cudaSuccess ||
           q != cudaDriverEntryPointSuccess || fn == nullptr)
         return MOE_ERR_CUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      g_encode.store(encode, std::memory_order_release);
     }
   }
-  const CUresult r = g_encode(map, dtype, (cuuint32_t)rank, base, dims, strides_bytes, box, elem_strides,
+  const CUresult r = encode(map, dtype, (cuuint32_t)rank, base, dims, strides_bytes, box, elem_strides,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;

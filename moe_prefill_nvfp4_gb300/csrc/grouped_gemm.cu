@@ -37,6 +37,7 @@
 // in-flight copies and MMAs, frees TMEM and exits.
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -536,15 +537,16 @@ using CfgL1 = Cfg<256, 3, 4, 1, 1>;
 
 template <class C>
 int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t stream) {
-  static int configured[64] = {0};
-  static int max_clusters[64][9] = {{0}};  // per device, per cluster width
+  // per-device caches of idempotent facts (several host threads may fill them concurrently)
+  static std::atomic<int> configured[64];
+  static std::atomic<int> max_clusters[64][9];  // per cluster width
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
-    configured[dev] = 1;
+    configured[dev].store(1, std::memory_order_release);
   }
   const int nsm = device_sm_count();
   if (nsm <= 0) return MOE_ERR_CUDA;
@@ -573,14 +575,14 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   int CL = 1, ncl_max = 0, widest = 0;
   for (int cl = gathered ? 8 : 2; cl >= 1; --cl) {
     if (groups % cl != 0) continue;
-    if (max_clusters[dev][cl] == 0) {
+    int n = max_clusters[dev][cl].load(std::memory_order_relaxed);
+    if (n == 0) {
       attr[0].val.clusterDim.x = cl;
       cfg.gridDim = dim3(cl * nsm);
-      int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
-      max_clusters[dev][cl] = n;
+      max_clusters[dev][cl].store(n, std::memory_order_relaxed);
     }
-    const int ctas = max_clusters[dev][cl] * cl;
+    const int ctas = n * cl;
     if (widest == 0) {
       widest = cl;
       const double rounds = (double)groups * ((args.R + C::BN_MAX - 1) / C::BN_MAX) / ctas;
@@ -594,7 +596,7 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
       break;
     }
   }
-  ncl_max = max_clusters[dev][CL];
+  ncl_max = max_clusters[dev][CL].load(std::memory_order_relaxed);
   attr[0].val.clusterDim.x = CL;
   const long long nbg = groups / CL;
   const long long max_groups = nbg * ((long long)args.E + (args.R + C::BN_MAX - 1) / C::BN_MAX);

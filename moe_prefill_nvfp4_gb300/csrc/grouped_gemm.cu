@@ -33,6 +33,10 @@
 //   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B] per block)
 //   13    activation producer (this CTA's share of each stage, multicast to the cluster)
 //   14-15 MMA issuers (one thread each, block 0 / block 1); warp 14 owns TMEM
+// When the activation ring and the TMEM A ring have the same depth, one "full" barrier per stage
+// gathers both producers (the activation bytes as TMA transaction bytes, the four warps of the
+// dequantising warpgroup as arrivals) and one commit per atom releases both, so the issuer waits
+// once per 64-k atom.
 // Every pipeline wait is bounded: on a timeout the CTA records MOE_DEVERR_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 
@@ -83,6 +87,7 @@ struct Cfg {
   static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
   static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
   // barriers: w_full[NW] w_empty[NW] a_full[NA] a_empty[NA] t_full[NT] t_empty[NT] d_full[ND] d_empty[ND]
+  // (t_full / t_empty idle when MERGED)
   // drain[NBLK]
   static constexpr int NBAR = 2 * NW + 2 * NA + 2 * NT + 2 * ND + NBLK;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -176,7 +181,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(w_empty(s), 8);
     }
     for (int s = 0; s < C::NA; ++s) {
-      mbar_init(a_full(s), 1);
+      // the slot is ready when its activation bytes have landed (one expect-tx arrival) and,
+      // when the rings coincide, the dequantisation warpgroup has filled the TMEM A stage (4)
+      mbar_init(a_full(s), C::MERGED ? 5 : 1);
       mbar_init(a_empty(s), CL * C::NBLK);  // one commit from every MMA warp of the cluster
     }
     for (int s = 0; s < NT; ++s) {
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(t_full(ts));
+          if (lane == 0) mbar_arrive(C::MERGED ? a_full(ts) : t_full(ts));
         }
         if (!ok) break;
       }
@@ -490,18 +497,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(d_empty(db), ((it / C::ND) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t idesc = make_idesc_bf16(BM, ti.bn);
+        const uint64_t bdesc0 = make_sdesc_sw128(sbase + C::OFF_ACT);
+        const uint32_t a_tmem0 = tmem_base + C::A_COL + b * 32;
         const uint32_t d_tmem = tmem_base + D_COL + (db * C::NBLK + b) * C::BN_MAX;
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % C::NA;
           const int ts = ai % NT;
           if (!mbar_wait(a_full(s), (ai / C::NA) & 1, s_abort, args.err)) { ok = false; break; }
-          if (!mbar_wait(t_full(ts), (ai / NT) & 1, s_abort, args.err)) { ok = false; break; }
+          if (!C::MERGED && !mbar_wait(t_full(ts), (ai / NT) & 1, s_abort, args.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t bsm = sbase + C::OFF_ACT + s * C::ACT_STAGE;
-          const uint32_t a_tmem = tmem_base + C::A_COL + ts * 32 * C::NBLK + b * 32;
-#pragma unroll
-          for (int kk = 0; kk < BKA / 16; ++kk)
-            mma_bf16_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(bsm + kk * 32), idesc, (kb | kk) != 0);
+          // the descriptor's start-address field is the byte address >> 4: a stage offset adds to it
+          const uint64_t bdesc = bdesc0 + (uint64_t)((s * C::ACT_STAGE) >> 4);
+          mma4_bf16_ts(d_tmem, a_tmem0 + ts * 32 * C::NBLK, bdesc, idesc, kb != 0);
           // One commit releases the activation slot in every CTA of the cluster; when the two
           // rings have the same depth it also releases the TMEM A stage (the dequantisation warps
           // then wait on the slot's barrier), otherwise a second commit does.
@@ -564,15 +571,14 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   cfg.numAttrs = 1;  // the occupancy queries below take the cluster attribute alone
   // cluster width: gathered rows are bound by the TMA gather4 issue rate of each SM (~80-150
   // cycles per 4-row copy), so wider multicast (any width up to 8 that divides the weight-block
-  // groups, not only powers of two) makes each tile cheaper; but wide clusters leave SMs idle
-  // (8-CTA clusters fit on 120 of 152 SMs, 6-CTA on 138), which costs a whole tile round when
-  // there are few rounds.  So: the widest width whose clusters cover >= 94% of the SMs, unless
-  // the launch has many tile rounds (>= 24 expected), where the widest width wins.  Contiguous
-  // rows in tiled boxes use pairs.
+  // groups, not only powers of two) makes each tile cheaper.  Wide clusters leave SMs idle (8-CTA
+  // clusters fit on 120 of 152 SMs, 6-CTA on 138), which measured as the lesser cost down to ~90%
+  // coverage: gathered rows take the widest width whose clusters cover >= 90% of the SMs.
+  // Contiguous rows in tiled boxes use pairs.
   const int nblocks = (args.N + BM - 1) / BM;
   const int groups = nblocks / C::NBLK;
   const bool gathered = args.gather != nullptr;
-  int CL = 1, ncl_max = 0, widest = 0;
+  int CL = 1, ncl_max = 0;
   for (int cl = gathered ? 8 : 2; cl >= 1; --cl) {
     if (groups % cl != 0) continue;
     int n = max_clusters[dev][cl].load(std::memory_order_relaxed);
@@ -582,16 +588,7 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
       if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
       max_clusters[dev][cl].store(n, std::memory_order_relaxed);
     }
-    const int ctas = n * cl;
-    if (widest == 0) {
-      widest = cl;
-      const double rounds = (double)groups * ((args.R + C::BN_MAX - 1) / C::BN_MAX) / ctas;
-      if (rounds >= 24.0) {
-        CL = cl;
-        break;
-      }
-    }
-    if (ctas * 100 >= nsm * 94) {
+    if (n * cl * 10 >= nsm * 9 || cl == 1) {
       CL = cl;
       break;
     }

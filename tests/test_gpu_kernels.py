@@ -246,17 +246,19 @@ def test_gemm_deterministic_and_bad_offsets():
     proj2.close()
 
 
-@pytest.mark.parametrize("T,E,k,N,identity", [(40, 16, 8, 512, False), (40, 16, 8, 512, True), (300, 24, 8, 512, False),
+@pytest.mark.parametrize("T,E,k,N,identity", [(40, 16, 8, 512, False), (40, 16, 8, 512, True), (80, 16, 8, 512, False),
+                                              (80, 16, 8, 512, True), (300, 24, 8, 512, False),
                                               (600, 4, 2, 512, False), (40, 16, 8, 384, False),
                                               (300, 24, 8, 384, False), (600, 4, 2, 384, False),
                                               (90, 12, 4, 2048, False)],
-                         ids=["64-row-pairs", "64-row-pairs-2acc-contiguous", "128-row-pairs", "128-row-pairs-300-mean",
-                              "64-row-odd-blocks", "128-row-odd-blocks", "256-row-odd-blocks",
-                              "64-row-pairs-cluster8"])
+                         ids=["48-row-pairs", "48-row-pairs-contiguous", "64-row-pairs", "64-row-pairs-2acc-contiguous",
+                              "128-row-pairs", "128-row-pairs-300-mean", "64-row-odd-blocks", "128-row-odd-blocks",
+                              "256-row-odd-blocks", "48-row-pairs-cluster8"])
 def test_gemm_each_tile_config(T, E, k, N, identity):
-    """Mean rows per expert ~20, ~100 and ~300 with even and odd numbers of 128-row weight
-    blocks select every token-tile configuration: 64-row tiles (pairs, pairs with two
-    accumulator buffers for contiguous rows, single blocks), 128-row tiles (pairs, single
+    """Mean rows per expert ~20, ~40, ~100 and ~300 with even and odd numbers of 128-row weight
+    blocks select every token-tile configuration: 48-row tiles (pairs, two accumulator buffers;
+    ~20 rows per expert, so some experts span two token tiles), 64-row tiles (pairs, pairs with
+    two accumulator buffers for contiguous rows, single blocks), 128-row tiles (pairs, single
     blocks), 256-row tiles (single blocks); 16 blocks make clusters of 8."""
     c = S.make_gemm_case(T=T, E=E, k=k, N=N, K=512, seed=23 + T + N)
     C, srt, proj = _gemm_case(c, identity=identity)
@@ -265,9 +267,10 @@ def test_gemm_each_tile_config(T, E, k, N, identity):
     proj.close()
 
 
-@pytest.mark.parametrize("T,E,k,I,big,identity", [(40, 16, 8, 256, False, False), (300, 24, 8, 256, True, False),
-                                                  (600, 4, 2, 128, True, False), (90, 12, 4, 768, False, True)],
-                         ids=["64-row", "128-row-clamped", "256-row-mean-clamped", "64-row-identity"])
+@pytest.mark.parametrize("T,E,k,I,big,identity", [(40, 16, 8, 256, False, False), (80, 16, 8, 256, False, False),
+                                                  (300, 24, 8, 256, True, False), (600, 4, 2, 128, True, False),
+                                                  (90, 12, 4, 768, False, True)],
+                         ids=["48-row", "64-row", "128-row-clamped", "256-row-mean-clamped", "48-row-identity"])
 def test_gemm_swiglu_fused(T, E, k, I, big, identity):
     """Gate/up GEMM with the clamped SwiGLU in the epilogue against the oracle's SwiGLU of the
     unrounded BF16-operand product: act = silu(min(g, L)) * clamp(u, -L, L), L = 7.  `big`

@@ -313,6 +313,9 @@ def run_gpu(args):
 
     # ---- roofline of the dominant kernel (largest mean stage time)
     off = ws[lay.expert_offsets:lay.expert_offsets + 4 * (E + 1)].view(torch.int32).cpu().numpy()
+    # stage intervals between the forward's 8 events; with a router (E <= 64) the router GEMM and the top-k
+    # are one launch ("route_topk" is then an empty interval), and with the fused SwiGLU the
+    # "swiglu" interval is empty (each interval carries the event node's own ~2 us)
     names = ["router_logits", "route_topk", "sort", "grouped_gemm_gate_up", "swiglu", "grouped_gemm_down", "combine"]
     mean_stage = stage_ms.mean(axis=0)
     dom = int(np.argmax(mean_stage))

@@ -335,8 +335,10 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *   stage_events NULL, or a host array of MOE_FWD_NUM_EVENTS cudaEvent_t (as void*) recorded
  *              on `stream` before the first stage and after each of the 7 stages (router,
  *              top-k, sort count, sort scatter, gate/up GEMM, SwiGLU, down GEMM, combine
- *              -> events 0..7 bracket them; a skipped router records event 1 = event 0, and
- *              with the fused SwiGLU (the default) event 5 = event 4).
+ *              -> events 0..7 bracket them; with a router and E <= 64 the router GEMM and
+ *              the top-k run as one launch (event 2 = event 1; the logits, ids and weights
+ *              equal those of moe_router_logits + moe_route_topk), a skipped router records event 1 = event
+ *              0, and with the fused SwiGLU (the default) event 5 = event 4).
  * The SwiGLU runs in the gate/up GEMM's epilogue (moe_w4a16_grouped_gemm_swiglu) unless
  * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.  With
  * MOE_FWD_SMALL_ROWS, chunks of T <= 8 rows take the small-row products (FP32 dequantised

@@ -539,16 +539,23 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   };
 
   ev(0);
-  const float* lg = logits_in;
-  if (w_router) {
-    rc = router_logits_launch(x, w_router, T, H, E, logits, st);
+  if (w_router && E <= kRouterTopkMaxE) {
+    // router GEMM and top-k in one launch (stage 1 -> 2 is empty): same results as the two
+    // standalone entry points
+    rc = router_topk_launch(x, w_router, T, H, E, router_bias, k, cfg->renormalize, cfg->routed_scale, logits, ids,
+                            wts, err, st);
     if (rc != MOE_OK) return rc;
-    lg = logits;
+    ev(1);
+  } else {
+    const float* lg = logits_in;
+    if (w_router) {
+      if ((rc = router_logits_launch(x, w_router, T, H, E, logits, st)) != MOE_OK) return rc;
+      lg = logits;
+    }
+    ev(1);
+    rc = route_topk_launch(lg, router_bias, T, E, k, cfg->renormalize, cfg->routed_scale, ids, wts, err, st);
+    if (rc != MOE_OK) return rc;
   }
-  ev(1);
-  if ((rc = route_topk_launch(lg, router_bias, T, E, k, cfg->renormalize, cfg->routed_scale, ids, wts, err, st)) !=
-      MOE_OK)
-    return rc;
   ev(2);
   if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st)) != MOE_OK) return rc;
   ev(3);

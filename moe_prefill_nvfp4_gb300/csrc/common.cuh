@@ -176,6 +176,12 @@ MOE_DEV uint32_t cluster_count_x() {
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
 }
+// Store to the shared memory of CTA `rank` of the cluster, at the offset of `local_addr` in ours.
+MOE_DEV void st_shared_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
 // All threads of all CTAs of the cluster (also orders this CTA's shared-memory writes, e.g.
 // mbarrier initialisation, before the other CTAs' later accesses).
 MOE_DEV void cluster_sync_all() {

@@ -53,6 +53,27 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// ... with thread-block clusters of cluster_x CTAs along x (grid.x a multiple of cluster_x)
+template <typename... KArgs, typename... Args>
+int launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // small-row products (small_rows.cu): at most 8 rows per expert, FP32 weights, BF16 out
 struct SmallRowsArgs {
   const uint16_t* A;
@@ -80,6 +101,12 @@ int shared_expert_launch(const uint16_t* x, int T, int H, int I, const uint16_t*
 
 // SIMT kernels (small_kernels.cu)
 int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st);
+// router logits + top-k in one launch (same results as router_logits_launch + route_topk_launch)
+// when E <= 64 (one cluster of E/8 CTAs per 4 rows); MOE_ERR_UNSUPPORTED_SHAPE otherwise
+constexpr int kRouterTopkMaxE = 64;
+int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, const float* bias, int k,
+                       int renormalize, float scale, float* logits, int32_t* ids, float* wts, int* err,
+                       cudaStream_t st);
 int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
                       int32_t* ids, float* wts, int* err, cudaStream_t st);
 int sort_segments(int R, int E);

@@ -26,15 +26,13 @@ namespace moe {
 
 constexpr int RL_TOK = 4, RL_EXP = 8, RL_WARPS = 8;
 
-__global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                                      const uint16_t* __restrict__ w, int T, int H,
-                                                                      int E, float* __restrict__ logits) {
-  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
-  griddep_wait();
-  griddep_launch_dependents();
+// The block's tile (tokens t0.., experts e0..): thread i * RL_EXP + j (< RL_TOK * RL_EXP)
+// receives output (t0 + i, e0 + j) in `out` and returns true.  Every thread of the block calls it
+// (it synchronises the block).  Shared by the standalone router kernel and the fused router +
+// top-k kernel, so both give the same bits.
+MOE_DEV bool router_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E, int t0,
+                         int e0, float (*s_red)[RL_TOK * RL_EXP], float& out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * RL_TOK;
-  const int e0 = blockIdx.y * RL_EXP;
   float v[RL_TOK * RL_EXP];
 #pragma unroll
   for (int i = 0; i < RL_TOK * RL_EXP; ++i) v[i] = 0.f;
@@ -77,10 +75,24 @@ __global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint
   }
   s_red[warp][lane] = v[0];  // output index lane = i * RL_EXP + j
   __syncthreads();
-  if (threadIdx.x < RL_TOK * RL_EXP) {
-    float a = 0.f;
+  if (threadIdx.x >= RL_TOK * RL_EXP) return false;
+  float a = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < RL_WARPS; ++ww) a += s_red[ww][threadIdx.x];
+  for (int ww = 0; ww < RL_WARPS; ++ww) a += s_red[ww][threadIdx.x];
+  out = a;
+  return true;
+}
+
+__global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                                      const uint16_t* __restrict__ w, int T, int H,
+                                                                      int E, float* __restrict__ logits) {
+  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t0 = blockIdx.x * RL_TOK;
+  const int e0 = blockIdx.y * RL_EXP;
+  float a;
+  if (router_tile(x, w, T, H, E, t0, e0, s_red, a)) {
     const int i = threadIdx.x / RL_EXP, j = threadIdx.x % RL_EXP;
     if (t0 + i < T && e0 + j < E) logits[(size_t)(t0 + i) * E + e0 + j] = a;
   }
@@ -98,17 +110,14 @@ constexpr int TOPK_WARPS = 8;
 
 MOE_DEV bool key_better(float ka, int ea, float kb, int eb) { return ka > kb || (ka == kb && ea < eb); }
 
+// One warp routes one row: top-k of (logit + bias) with ties to the lower expert index, weights
+// from the unbiased logits (softmax over the k picks, or over all experts).  `lrow` may point to
+// global or shared memory.  Shared by the standalone top-k kernel and the fused router + top-k
+// kernel.
 template <int NPL>
-__global__ void __launch_bounds__(TOPK_WARPS * 32)
-    route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
-                      int renormalize, float routed_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
-                      int* err) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * TOPK_WARPS + warp;
-  if (row >= T) return;
-  const float* lrow = logits + (size_t)row * E;
+MOE_DEV void topk_row(const float* lrow, const float* __restrict__ bias, int E, int k, int renormalize,
+                      float routed_scale, int32_t* __restrict__ ids_row, float* __restrict__ wts_row, int* err) {
+  const int lane = threadIdx.x & 31;
   float val[NPL], key[NPL];
   bool nan_seen = false;
 #pragma unroll
@@ -175,9 +184,23 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32)
     w = mine ? expf(l - m) / sum : 0.f;
   }
   if (mine) {
-    ids[(size_t)row * k + lane] = my_id;
-    wts[(size_t)row * k + lane] = w * routed_scale;
+    ids_row[lane] = my_id;
+    wts_row[lane] = w * routed_scale;
   }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(TOPK_WARPS * 32)
+    route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+                      int renormalize, float routed_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+                      int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5;
+  const int row = blockIdx.x * TOPK_WARPS + warp;
+  if (row >= T) return;
+  topk_row<NPL>(logits + (size_t)row * E, bias, E, k, renormalize, routed_scale, ids + (size_t)row * k,
+                wts + (size_t)row * k, err);
 }
 
 int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
@@ -194,6 +217,53 @@ int route_topk_launch(const float* logits, const float* bias, int T, int E, int 
   if (npl <= 16) return MOE_TOPK_CASE(16);
   return MOE_TOPK_CASE(32);
 #undef MOE_TOPK_CASE
+}
+
+// ------------------------------------------------------------------------------------------------
+// router logits + top-k in one launch (the forward's routing when it owns the router GEMM and
+// E <= 64): a cluster of ceil(E / 8) CTAs takes 4 rows; CTA r computes the 4 x 8 logit tile of
+// experts 8r.. exactly as the standalone router kernel does, writes it to global memory and into
+// the shared memory of CTA 0 of the cluster; after the cluster barrier, warps 0..3 of CTA 0 route
+// one row each with the standalone top-k routine.  Same bits as the two separate launches, one
+// launch and one HBM round trip of the logits fewer.
+
+template <int NPL>
+__global__ void __launch_bounds__(RL_WARPS * 32)
+    router_topk_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
+                       const float* __restrict__ bias, int k, int renormalize, float routed_scale,
+                       float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int* err) {
+  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
+  __shared__ float s_log[RL_TOK][32 * NPL];  // CTA 0's copy receives every CTA's tile
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t0 = blockIdx.y * RL_TOK;
+  const int e0 = blockIdx.x * RL_EXP;  // blockIdx.x == rank in the cluster
+  float a;
+  if (router_tile(x, w, T, H, E, t0, e0, s_red, a)) {
+    const int i = threadIdx.x / RL_EXP, e = e0 + threadIdx.x % RL_EXP;
+    if (e < E) {
+      if (t0 + i < T) logits[(size_t)(t0 + i) * E + e] = a;
+      st_shared_cluster_f32(smem_u32(&s_log[i][e]), 0, a);
+    }
+  }
+  cluster_sync_all();  // the cluster's tiles are in CTA 0's shared memory
+  const int warp = threadIdx.x >> 5;
+  if (cluster_ctarank() == 0 && warp < RL_TOK && t0 + warp < T)
+    topk_row<NPL>(s_log[warp], bias, E, k, renormalize, routed_scale, ids + (size_t)(t0 + warp) * k,
+                  wts + (size_t)(t0 + warp) * k, err);
+}
+
+int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, const float* bias, int k,
+                       int renormalize, float scale, float* logits, int32_t* ids, float* wts, int* err,
+                       cudaStream_t st) {
+  if (E > kRouterTopkMaxE) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int groups = (E + RL_EXP - 1) / RL_EXP;  // cluster size, <= 8
+  const dim3 grid(groups, (T + RL_TOK - 1) / RL_TOK);
+  if (E <= 32)
+    return launch_pdl_cluster(router_topk_kernel<1>, grid, dim3(RL_WARPS * 32), 0, st, groups, x, w, T, H, E, bias,
+                              k, renormalize, scale, logits, ids, wts, err);
+  return launch_pdl_cluster(router_topk_kernel<2>, grid, dim3(RL_WARPS * 32), 0, st, groups, x, w, T, H, E, bias, k,
+                            renormalize, scale, logits, ids, wts, err);
 }
 
 // ------------------------------------------------------------------------------------------------

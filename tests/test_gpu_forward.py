@@ -329,3 +329,32 @@ def test_shared_expert_on_a_second_stream():
     torch.cuda.synchronize()
     assert torch.equal(db.out.view(torch.int16), serial.view(torch.int16))
     db.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,H,E,k,renorm,bias", [(37, 512, 5, 2, True, False), (130, 1024, 40, 8, False, True),
+                                                 (66, 512, 72, 4, True, True), (256, 2048, 64, 8, True, True)],
+                         ids=["E5-cluster1-ragged", "E40-cluster5-no-renorm-bias", "E72-separate-launches",
+                              "c1-shape-cluster8-bias"])
+def test_forward_routing_equals_standalone_entry_points(T, H, E, k, renorm, bias):
+    """With a router and E <= 64, the forward runs the router GEMM and the top-k as one launch (a
+    cluster of ceil(E/8) CTAs per 4 rows); its logits, ids and weights must be the bits of
+    moe_router_logits followed by moe_route_topk (the same tile routine and the same per-row
+    selection routine).  T % 4 != 0 and E % 8 != 0 exercise the partial tiles; E = 72 takes the
+    two separate launches."""
+    c = S.make_block_case(T=T, H=H, I=256, E=E, k=k, routing="router", seed=61 + T + E)
+    c.renormalize = 1 if renorm else 0
+    db = DeviceBlock(c)
+    b = torch.linspace(-0.05, 0.05, E, dtype=torch.float32, device="cuda") if bias else None
+    moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, w_router=db.router_w, router_bias=b,
+                            out=db.out)
+    torch.cuda.synchronize()
+    st = db.stages()
+    lg = moe.moe_router_logits(db.x, db.router_w)
+    ids, wts = moe.moe_route_topk(lg, k, bias=b, renormalize=renorm, routed_scale=c.routed_scale)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    np.testing.assert_array_equal(st["logits"].view(np.uint32), lg.cpu().numpy().view(np.uint32))
+    np.testing.assert_array_equal(st["ids"], ids.cpu().numpy())
+    np.testing.assert_array_equal(st["wts"].view(np.uint32), wts.cpu().numpy().view(np.uint32))
+    db.close()

@@ -29,7 +29,9 @@
 //
 // Warp roles (16 warps):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 -> shared staging -> 16-byte global stores
-//   4-11  dequantisation, two warpgroups taking alternate 64-k sub-stages
+//   4-11  dequantisation, two warpgroups taking alternate 64-k sub-stages (the 128-row token
+//         tiles use one warpgroup, warps 4-7: measured 4-5% faster there, the second one mostly
+//         competes with the MMA issuers for issue slots; warps 8-11 then idle)
 //   12    weight producer (TMA: packed [128 x 128 B] swizzled + scales [128 x 16 B] per block)
 //   13    activation producer (this CTA's share of each stage, multicast to the cluster)
 //   14-15 MMA issuers (one thread each, block 0 / block 1); warp 14 owns TMEM
@@ -62,15 +64,17 @@ constexpr int ID_BOX_ROWS = 16;  // rows per tiled box when the A rows are conti
 
 // BN_MAX: token-tile width (MMA N, at most 256); NA/NW: activation/weight ring depths;
 // ND: accumulator buffers per block (2 lets the epilogue of one tile overlap the next tile's
-// MMAs); NBLK: 128-row weight blocks per CTA.  TMEM: ND*NBLK*BN_MAX accumulator columns, the
-// rest holds NT A stages of 32*NBLK columns (64 k of every block).
-template <int BN_MAX_, int NA_, int NW_, int ND_, int NBLK_>
+// MMAs); NBLK: 128-row weight blocks per CTA; NDQ: dequantising warpgroups (1 or 2).  TMEM:
+// ND*NBLK*BN_MAX accumulator columns, the rest holds NT A stages of 32*NBLK columns (64 k of
+// every block).
+template <int BN_MAX_, int NA_, int NW_, int ND_, int NBLK_, int NDQ_ = 2>
 struct Cfg {
   static constexpr int BN_MAX = BN_MAX_;
   static constexpr int NA = NA_;
   static constexpr int NW = NW_;
   static constexpr int ND = ND_;
   static constexpr int NBLK = NBLK_;
+  static constexpr int NDQ = NDQ_;
   static constexpr int ROWS = BM * NBLK;
   static constexpr int A_COL = ND * NBLK * BN_MAX;
   static constexpr int NT = (TMEM_COLS - A_COL) / (32 * NBLK);
@@ -96,6 +100,7 @@ struct Cfg {
   static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256 && A_COL % 32 == 0 && NT >= 2, "token tile / TMEM columns");
   static_assert(OFF_PK % 1024 == 0 && ACT_STAGE % 1024 == 0, "swizzled buffers need 1024-byte alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
+  static_assert(NDQ == 1 || NDQ == 2, "dequantising warpgroups");
 };
 
 struct TileInfo {
@@ -342,8 +347,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-  } else if (warp < 12) {
+  } else if (warp < 4 + 4 * C::NDQ) {
     // ------------------------------------------------------------------ dequantisation
+    // Two warpgroups take alternate 64-k sub-stages of each weight stage (warpgroup wg: subs wg,
+    // wg + 2); one warpgroup takes all four in order, two per pass over the stage.  Every pass
+    // arrives once on the stage's "empty" barrier (8 arrivals per stage either way).
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -353,7 +361,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int g = cid; ok && g < total; g += ncl) {
       const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
       const float s2 = args.scale2[ti.e];
-      for (int ks = 0; ks < KW; ++ks, ++wi) {
+      for (int ks = 0; ok && ks < KW; ++ks, ++wi)
+      for (int pass = 0; pass < 2 / C::NDQ; ++pass) {
         const int s = wi % C::NW;
         if (!warp_wait(w_full(s), (wi / C::NW) & 1, s_abort, args.err)) { ok = false; break; }
         uint4 chunk[C::NBLK][4];
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           scv[b] = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + s * C::SC_STAGE + wr * 16);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int sub = wg + 2 * h;
+            const int sub = C::NDQ == 2 ? wg + 2 * h : 2 * pass + h;
             chunk[b][2 * h] = *reinterpret_cast<const uint4*>(pk + (((2 * sub) ^ (wr & 7)) << 4));
             chunk[b][2 * h + 1] = *reinterpret_cast<const uint4*>(pk + (((2 * sub + 1) ^ (wr & 7)) << 4));
           }
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(w_empty(s));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int sub = wg + 2 * h;
+          const int sub = C::NDQ == 2 ? wg + 2 * h : 2 * pass + h;
           const int tix = wi * 4 + sub;
           const int ts = tix % NT;
           if (!warp_wait(C::MERGED ? a_empty(ts) : t_empty(ts), ((tix / NT) & 1) ^ 1, s_abort, args.err)) {
@@ -487,8 +496,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = max(0, ai - C::NA); j < ai; ++j) mbar_wait_drain(a_full(j % C::NA), (j / C::NA) & 1);
   } else {
     // ------------------------------------------------------------------ MMA issuers
-    const int b = warp - WARP_MMA;  // weight block of this issuer
-    if (lane == 0 && b < C::NBLK) {
+    const int b = warp - WARP_MMA;  // weight block of this issuer (b < 0: a warp without a role)
+    if (lane == 0 && b >= 0 && b < C::NBLK) {
       int ai = 0, it = 0;
       bool ok = true;
       for (int g = cid; ok && g < total; g += ncl, ++it) {
@@ -538,7 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 using CfgT2 = Cfg<48, 5, 4, 2, 2>;   // NT = 5; two accumulator buffers (mean rows per expert <= 32)
 using CfgS2 = Cfg<64, 6, 4, 1, 2>;   // NT = 6
 using CfgS2D = Cfg<64, 4, 4, 2, 2>;  // NT = 4; two accumulator buffers (contiguous rows)
-using CfgM2 = Cfg<128, 4, 3, 1, 2>;  // NT = 4
+using CfgM2 = Cfg<128, 4, 3, 1, 2, 1>;  // NT = 4; one dequantising warpgroup
 using CfgS1 = Cfg<64, 12, 6, 2, 1>;  // NT = 12
 using CfgM1 = Cfg<128, 8, 4, 2, 1>;  // NT = 8
 using CfgL1 = Cfg<256, 3, 4, 1, 1>;

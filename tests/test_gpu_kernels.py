@@ -94,8 +94,8 @@ def _check_sort(ids_np, E):
         np.testing.assert_array_equal(got[key].cpu().numpy().reshape(ref[key].shape), ref[key], err_msg=key)
 
 
-@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (64, 8, 16), (2048, 8, 160), (8192, 8, 160), (16384, 8, 160),
-                                   (777, 3, 1000), (100, 32, 40)])
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (64, 8, 16), (256, 8, 64), (256, 8, 512), (2048, 8, 160),
+                                   (8192, 8, 160), (16384, 8, 160), (777, 3, 1000), (100, 32, 40)])
 def test_sort_bit_exact(T, k, E):
     g = np.random.default_rng(T + E)
     ids = np.argsort(g.random((T, E)), axis=1)[:, :k].astype(np.int32)
@@ -110,6 +110,16 @@ def test_sort_skewed_and_unfilled():
     ids2 = g.integers(0, 12, (333, 4)).astype(np.int32)
     ids2[g.random((333, 4)) < 0.1] = -1
     _check_sort(ids2, 12)
+
+
+def test_sort_single_block_one_bucket_and_tail():
+    """R = 2048 slots (the single-block sort's maximum) all in one expert, then every slot but the
+    last in the -1 tail: the per-warp counts reach 64 and the bucket prefix 2048."""
+    ids = np.full((256, 8), 3, np.int32)
+    _check_sort(ids, 5)
+    ids[:] = -1
+    ids[-1, -1] = 4
+    _check_sort(ids, 5)
 
 
 def test_sort_flags_out_of_range_id():

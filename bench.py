@@ -358,9 +358,11 @@ def run_gpu(args):
                   "stage events, replayed one step at a time",
         "roofline": roof,
         "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
-        # router (when given router weights), top-k, sort, gate/up GEMM with the fused SwiGLU,
-        # down GEMM, combine (+ the shared expert's SwiGLU; its GEMMs are cuBLAS kernels)
-        "gpu_launches": ((7 if wr is not None else 6) + (1 if sh is not None else 0)) * args.steps,
+        # routing (router GEMM + top-k as one launch for E <= 64, else two; top-k alone on given
+        # logits), sort (one launch up to 2048 slots, else two), gate/up GEMM with the fused
+        # SwiGLU, down GEMM, combine (+ the shared expert's SwiGLU; its GEMMs are cuBLAS kernels)
+        "gpu_launches": (((2 if E > 64 else 1) if wr is not None else 1) + (1 if T * k <= 2048 else 2) + 3
+                         + (1 if sh is not None else 0)) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 4),
     }

@@ -349,10 +349,13 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
                         const moe_expert_table* w_down, void* ws, size_t ws_bytes, uint16_t* out,
                         const uint16_t* shared_out, void* shared_ready, void* const* stage_events, void* stream);
 
-/* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection). */
+/* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection).
+ * `ready`: INT32 [E + 1], per-expert counters through which the down GEMM starts on an expert as
+ * soon as the gate/up GEMM has stored its activation rows, and the down GEMM's dynamic tile
+ * counter (cleared by the sort on every call). */
 typedef struct {
-  size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, G,
-      act, Y, total;
+  size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, ready,
+      G, act, Y, total;
 } moe_workspace_layout_t;
 int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_workspace_layout_t* layout);
 

@@ -58,7 +58,7 @@ class MoePrefillConfig(ctypes.Structure):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "ids", "wts", "sorted_token_ids", "sorted_expert_ids",
-                                               "expert_offsets", "token_to_perm", "sort_scratch", "G", "act", "Y",
+                                               "expert_offsets", "token_to_perm", "sort_scratch", "ready", "G", "act", "Y",
                                                "total")]
 
 

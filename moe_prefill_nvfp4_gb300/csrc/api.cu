@@ -300,7 +300,8 @@ int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t*
 // I = swiglu_half = N / 2 writing BF16 act [R, ldc >= I].
 static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids, const moe_expert_table* W,
                         const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st,
-                        int swiglu_half = 0, float limit = 0.f) {
+                        int swiglu_half = 0, float limit = 0.f, int* ready_out = nullptr,
+                        const int* ready_in = nullptr, int ready_need = 0, int* tile_counter = nullptr) {
   if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
   if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (swiglu_half && (c_dtype != MOE_DTYPE_BF16 || W->N != 2 * swiglu_half || swiglu_half % 128 != 0))
@@ -329,6 +330,10 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.err = device_error_word();
   a.swiglu_half = swiglu_half;
   a.limit = limit;
+  a.ready_out = ready_out;
+  a.ready_in = ready_in;
+  a.ready_need = ready_need;
+  a.tile_counter = tile_counter;
   return grouped_gemm_launch(a, A, a_rows, lda, st);
 }
 
@@ -480,6 +485,7 @@ int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspac
   L->expert_offsets = take((E + 1) * 4);
   L->token_to_perm = take(R * 4);
   L->sort_scratch = take(sort_scratch_bytes((int)R, (int)E));
+  L->ready = take((E + 1) * 4);
   L->G = take((c->flags & MOE_FWD_SEPARATE_SWIGLU) ? R * 2 * I * 2 : 0);
   L->act = take(R * I * 2);
   L->Y = take(R * H * 2);
@@ -557,10 +563,16 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     if (rc != MOE_OK) return rc;
   }
   ev(2);
-  if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st)) != MOE_OK) return rc;
+  // The fused-SwiGLU tensor-core path runs the down GEMM alongside the gate/up GEMM's last tiles:
+  // the down GEMM loads an expert's activation rows once every gate/up CTA tile of them is stored
+  // (per-expert counters ready[0..E)), and its clusters take tiles dynamically (counter ready[E]),
+  // so the SMs the gate/up launch leaves early take more of the down work.  The sort clears them.
+  const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
+  const bool overlap = !small && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
+  int32_t* ready = overlap ? reinterpret_cast<int32_t*>(base + L.ready) : nullptr;
+  if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, E + 1)) != MOE_OK) return rc;
   ev(3);
   // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
-  const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   if (small) {
     rc = gemv_checked(x, T, H, sti, w_gate_up, off, R, act, I, I, cfg->swiglu_limit, st);
     if (rc != MOE_OK) return rc;
@@ -570,13 +582,16 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
   } else {
-    rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit);
+    // one producer CTA tile per 128 activation columns (a gate block and its up block)
+    rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit, ready,
+                      nullptr, I / 128);
     if (rc != MOE_OK) return rc;
     ev(4);
   }
   ev(5);
   rc = small ? gemv_checked(act, R, I, nullptr, w_down, off, R, Y, H, 0, 0.f, st)
-             : gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st);
+             : gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st, 0, 0.f, nullptr, ready,
+                            I / 128, ready ? ready + E : nullptr);
   if (rc != MOE_OK) return rc;
   ev(6);
   if (shared_ready && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(shared_ready), 0) != cudaSuccess)

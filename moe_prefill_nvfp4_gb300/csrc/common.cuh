@@ -92,6 +92,69 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, 
   }
 }
 
+// Waits until the counter at p (global memory, written by other CTAs or grids) reaches `need`,
+// with acquire ordering at GPU scope; the same bounds as mbar_wait.
+MOE_DEV bool wait_counter_geq(const int* p, int need, volatile int* abort_flag, int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
+// Adds v to the counter at p with release ordering at GPU scope.
+MOE_DEV void counter_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses (e.g. an acquire of data that other threads
+// stored) before its later async-proxy (TMA) accesses of global memory.
+MOE_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Cluster-scope mbarrier operations on the barrier at the same shared offset in CTA `rank`:
+// arrive with release (orders this thread's earlier st.shared::cluster), and a local wait with
+// acquire at cluster scope.
+MOE_DEV void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+MOE_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+MOE_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+MOE_DEV void st_shared_cluster_u32(uint32_t local_addr, uint32_t rank, uint32_t v) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
 // Wait used while unwinding: bounded, ignores the abort flag.
 MOE_DEV bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();

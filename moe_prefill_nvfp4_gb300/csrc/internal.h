@@ -25,6 +25,17 @@ struct GemmArgs {
   // and C is the BF16 activation [R, swiglu_half]
   int swiglu_half;
   float limit;
+  // Overlap of the two GEMMs of one forward (all NULL = off).  Producer: after its stores of a
+  // tile each of the 4 epilogue warps adds the tile's row count to ready_out[expert]; after
+  // zero-filling rows of an absent expert each adds their count times ready_need.  Consumer:
+  // expert e's A rows are loaded only once ready_in[e] >= rows_e * ready_need * 4 (ready_need =
+  // the producer's CTA tiles covering one row); its clusters take tiles dynamically from
+  // *tile_counter (zero at launch), so the CTAs that start early, on SMs the producer has left,
+  // take more tiles; it waits for the previous grid only at its end.
+  int* ready_out;
+  const int* ready_in;
+  int ready_need;
+  int* tile_counter;
 };
 
 // Host: encode a tiled tensor map through the driver entry point (no libcuda link needed).
@@ -113,9 +124,10 @@ int sort_segments(int R, int E);
 size_t sort_scratch_bytes(int R, int E);
 // The stable sort: one block when R <= 2048 (cnt unused), else histogram + scatter kernels over
 // segments of 2048 slots with the per-segment counts in cnt (sort_scratch_bytes).
+// zero: NULL, or an INT32 array of zero_n elements the sort clears (the forward's overlap counters)
 int sort_launch(const int32_t* ids, int R, int k, int E, int32_t* cnt, int32_t* sorted_token_ids,
                 int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, int* err,
-                cudaStream_t st);
+                cudaStream_t st, int32_t* zero = nullptr, int zero_n = 0);
 int swiglu_launch(const uint16_t* gate, const uint16_t* up, int64_t rows, int64_t width, int64_t ld_in, uint16_t* out,
                   int64_t ld_out, float limit, cudaStream_t st);
 int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, const uint16_t* shared_out, int T, int k,

@@ -312,11 +312,14 @@ __global__ void __launch_bounds__(SORT_THREADS)
 __global__ void __launch_bounds__(SORT_THREADS)
     sort_scatter_kernel(const int32_t* __restrict__ ids, int R, int k, int E, int S, const int32_t* __restrict__ cnt,
                         int32_t* __restrict__ sorted_token_ids, int32_t* __restrict__ sorted_expert_ids,
-                        int32_t* __restrict__ expert_offsets, int32_t* __restrict__ token_to_perm) {
+                        int32_t* __restrict__ expert_offsets, int32_t* __restrict__ token_to_perm,
+                        int32_t* __restrict__ zero, int zero_n) {
   extern __shared__ int s_mem[];
   griddep_wait();
   griddep_launch_dependents();
   const int NB = E + 1;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_n; i += SORT_THREADS) zero[i] = 0;
   int* s_base = s_mem;                                              // [NB]
   int16_t* s_wcnt = reinterpret_cast<int16_t*>(s_base + NB);        // [SORT_WARPS][NB]
   int16_t* s_lpos = s_wcnt + SORT_WARPS * NB;                       // [SORT_SEG]
@@ -414,11 +417,12 @@ __global__ void __launch_bounds__(SORT_THREADS)
 __global__ void __launch_bounds__(SORT_THREADS)
     sort_single_kernel(const int32_t* __restrict__ ids, int R, int k, int E, int32_t* __restrict__ sorted_token_ids,
                        int32_t* __restrict__ sorted_expert_ids, int32_t* __restrict__ expert_offsets,
-                       int32_t* __restrict__ token_to_perm, int* err) {
+                       int32_t* __restrict__ token_to_perm, int32_t* __restrict__ zero, int zero_n, int* err) {
   extern __shared__ int s_mem[];
   griddep_wait();
   griddep_launch_dependents();
   const int NB = E + 1;
+  for (int i = threadIdx.x; i < zero_n; i += SORT_THREADS) zero[i] = 0;
   int* s_base = s_mem;                                              // [NB]
   int16_t* s_wcnt = reinterpret_cast<int16_t*>(s_base + NB);        // [SORT_WARPS][NB]
   int16_t* s_lpos = s_wcnt + SORT_WARPS * NB;                       // [SORT_SEG]
@@ -500,16 +504,17 @@ static size_t scatter_smem(int E) {
 
 int sort_launch(const int32_t* ids, int R, int k, int E, int32_t* cnt, int32_t* sorted_token_ids,
                 int32_t* sorted_expert_ids, int32_t* expert_offsets, int32_t* token_to_perm, int* err,
-                cudaStream_t st) {
+                cudaStream_t st, int32_t* zero, int zero_n) {
+  if (zero == nullptr) zero_n = 0;
   if (R <= SORT_SEG)
     return launch_pdl(sort_single_kernel, dim3(1), dim3(SORT_THREADS), scatter_smem(E), st, ids, R, k, E,
-                      sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, err);
+                      sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, zero, zero_n, err);
   const int S = sort_segments(R, E);
   const int rc = launch_pdl(sort_hist_kernel, dim3(S), dim3(SORT_THREADS), (E + 1) * sizeof(int), st, ids, R, E, S,
                             cnt, err);
   if (rc != MOE_OK) return rc;
   return launch_pdl(sort_scatter_kernel, dim3(S), dim3(SORT_THREADS), scatter_smem(E), st, ids, R, k, E, S, cnt,
-                    sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm);
+                    sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, zero, zero_n);
 }
 
 // ------------------------------------------------------------------------------------------------

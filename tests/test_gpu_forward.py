@@ -112,6 +112,18 @@ def test_absent_expert_block(separate):
     _check_full(c, separate)
 
 
+def test_expert_absent_only_in_gate_up():
+    """The down GEMM starts on an expert once the gate/up GEMM has published all its activation
+    rows; for an expert the gate/up table lacks, those rows are the zero rows that launch writes,
+    and they must be published too (the down GEMM would otherwise wait out its 2 s bound)."""
+    c = S.make_block_case(T=64, H=256, I=256, E=6, k=2, routing="biased", seed=35)
+    c.gate_up.packed[3] = None
+    c.gate_up.scales[3] = None
+    assert (c.logits.argsort(axis=1)[:, -2:] == 3).any()  # expert 3 receives rows
+    _check_full(c)
+    assert moe.moe_get_device_error() == 0
+
+
 @pytest.mark.parametrize("flags", [0, 2], ids=["tensor-core-gemms", "small-row-products"])
 def test_eight_row_chunk(flags):
     """T = 8 at GLM-like widths: the default tensor-core GEMMs, and the small-row products that

@@ -340,7 +340,11 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *              equal those of moe_router_logits + moe_route_topk), a skipped router records event 1 = event
  *              0, and with the fused SwiGLU (the default) event 5 = event 4).
  * The SwiGLU runs in the gate/up GEMM's epilogue (moe_w4a16_grouped_gemm_swiglu) unless
- * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.  With
+ * cfg->flags has MOE_FWD_SEPARATE_SWIGLU; then G is written to the workspace first.  With the
+ * fused SwiGLU the down GEMM overlaps the gate/up GEMM's last tiles: it starts on an expert once
+ * the gate/up GEMM has published that expert's activation rows through the workspace's `ready`
+ * counters, and takes its tiles dynamically (bounded waits; a gate/up launch that fails to
+ * publish makes the down launch record MOE_DEVERR_TIMEOUT after 2 s instead of hanging).  With
  * MOE_FWD_SMALL_ROWS, chunks of T <= 8 rows take the small-row products (FP32 dequantised
  * weights, as the pages' decode GEMV) instead of the tensor-core GEMMs.
  */

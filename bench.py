@@ -153,17 +153,30 @@ def replica_throughput(n_ranks: int, rows_per_step: int, steps: int, max_ms: flo
 GEMM_SOURCES = ("grouped_gemm.cu", "common.cuh", "internal.h")
 
 
-def measured_traffic(workload: str, launch: str):
-    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
-    kernel's sources changed since those counters were taken (or the workload was not captured)."""
+def gemm_sources_digest() -> str:
+    """SHA-256 of the grouped GEMM's sources (concatenated in GEMM_SOURCES order) with C/C++
+    comments removed and whitespace runs collapsed: an edit of a comment keeps the counters valid,
+    any change of code does not."""
     import hashlib
+    import re
 
     csrc = os.path.join(ROOT, "moe_prefill_nvfp4_gb300", "csrc")
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    digest = h.hexdigest()
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        # string literals of these files hold inline PTX, whose "//" never starts a comment there;
+        # keep literals, drop comments
+        tok = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+        text = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, launch: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
+    kernel's sources changed since those counters were taken (or the workload was not captured)."""
+    digest = gemm_sources_digest()
     path = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.txt")
     if not os.path.exists(path):
         return None

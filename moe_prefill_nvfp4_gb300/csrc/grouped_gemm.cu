@@ -19,9 +19,12 @@
 //
 // Tile order is (expert, n-block group, token block) with the token block fastest, so the
 // clusters that share one expert's weights run at the same time and repeats hit L2: each
-// expert's packed weights and scales are read from HBM once per launch.  The static round-robin
-// walk over clusters is the persistent scheduler: it is driven by expert_offsets on the device,
-// balances skew by splitting heavy experts into many token blocks, and needs no host round trip.
+// expert's packed weights and scales are read from HBM once per launch.  The persistent
+// scheduler is driven by expert_offsets on the device (no host round trip) and balances skew by
+// splitting heavy experts into many token blocks.  By default it is a static round-robin walk
+// over clusters; a launch that consumes a producer GEMM's output in the same forward (the down
+// GEMM after the gate/up GEMM) claims tiles dynamically instead, so that its clusters that start
+// early, on SMs the producer has already left, take more of the work (see tile_at below).
 //
 // A CTA owns NBLK (1 or 2) adjacent 128-row weight blocks that share the activation tile; each
 // block has its own accumulator and its own MMA-issuing warp (one thread issues an MMA only every

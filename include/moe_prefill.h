@@ -326,7 +326,10 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *              space only with MOE_FWD_SEPARATE_SWIGLU).  Its
  *              contents after the call: logits, ids, wts, the sort arrays, G, act, Y, at the
  *              offsets moe_workspace_layout reports.
- *   out        device BF16 [T, H]
+ *   out        BF16 [T, H] in memory the device can store to: device memory, or page-locked
+ *              host memory (the combine then writes the result straight to the host; no copy
+ *              follows).  Other pointers: MOE_ERR_INVALID_ARG, unless the device has pageable
+ *              memory access.
  *   shared_out device BF16 [T, H] or NULL: the shared expert's output, added in the combine
  *              (moe_shared_expert_forward)
  *   shared_ready NULL, or a cudaEvent_t (as void*) the stream waits for right before the

@@ -68,6 +68,28 @@ int ensure_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// True when kernels on the current device may store through p: device or managed memory,
+// page-locked host memory (unified addressing maps it at the same address), or any host memory
+// on a device with pageable memory access (a coherent CPU-GPU node).  The pointer query is not a
+// stream operation, so it runs in relaxed capture mode while a CUDA graph is being captured.
+bool device_accessible(const void* p) {
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return false;
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer == p;
+  int pageable = 0;
+  const int d = current_device();
+  return d >= 0 && cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, d) == cudaSuccess &&
+         pageable != 0;
+}
+
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
@@ -519,6 +541,7 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   rc = ensure_device();
   if (rc != MOE_OK) return rc;
   if (current_device() != w_gate_up->device || current_device() != w_down->device) return MOE_ERR_INVALID_ARG;
+  if (!device_accessible(out)) return MOE_ERR_INVALID_ARG;
 
   cudaStream_t st = as_stream(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);

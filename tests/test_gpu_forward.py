@@ -244,6 +244,30 @@ def test_forward_graph_capture_replay():
     db.close()
 
 
+def test_output_into_pinned_host_memory():
+    """out may be page-locked host memory: the combine stores the result there directly, eagerly
+    and inside a captured graph, bit-identical to the device-memory result."""
+    c = S.make_block_case(T=96, H=512, I=256, E=12, k=4, routing="biased", seed=36)
+    db = DeviceBlock(c)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        db.forward(stream=s)
+    torch.cuda.synchronize()
+    ref = db.out.cpu()
+    host = torch.zeros(c.T, c.H, dtype=torch.bfloat16).pin_memory()
+    moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, logits=db.logits, out=host, stream=s)
+    s.synchronize()
+    assert torch.equal(host.view(torch.int16), ref.view(torch.int16))
+    host.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, logits=db.logits, out=host, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(host.view(torch.int16), ref.view(torch.int16))
+    db.close()
+
+
 def test_stage_events_inside_graph_capture():
     """Stage events recorded during capture become timestamp nodes: each replay records them."""
     c = S.make_block_case(T=96, H=512, I=256, E=12, k=4, routing="biased", seed=35)

@@ -4,8 +4,9 @@
 //
 // Each is one launch over all rows (the pages measured per-row launches of top-k and combine
 // as pure launch overhead: "glm5next_mlp/forward.rs", forward_moe comments), with 16-byte
-// vector loads/stores on the row-major BF16 tensors and warp-level primitives (ballot,
-// shuffles) for selection, counting and the per-expert prefix.
+// vector loads/stores on the row-major BF16 tensors, the router's dense contraction on the
+// tensor cores (warp-level MMAs), and warp-level primitives (reductions, ballot, shuffles) for
+// selection, counting and the per-expert prefix.
 
 #include <cuda_bf16.h>
 
@@ -19,88 +20,99 @@ namespace moe {
 // ------------------------------------------------------------------------------------------------
 // router logits: logits[t, e] = sum_h x[t, h] * w[e, h]  (BF16 in, FP32 accumulate and out)
 //
-// A block owns a 4-token x 8-expert tile and its 8 warps split h: every lane loads one 16-byte
-// vector of each of the 12 rows per 2048 h up front (one memory round trip), keeps 32 FP32
-// partial sums, and the 32 sums are reduce-scattered across the warp (lane j ends with output
-// j) and then added over the warps in a fixed order: deterministic.
+// A cluster of `cl` CTAs owns a 16-token x 64-expert tile and its 8 * cl warps split h into
+// 32-element super-steps (warp gw of the cluster takes super-steps gw, gw + 8 cl, ...).  Per
+// super-step a warp runs two BF16 tensor-core MMAs (m16n8k16, FP32 accumulate) on each of the
+// tile's eight 8-expert column groups.  The order of k inside an MMA is free as long as x and w
+// use the same one: lane (g, q) loads one 16-byte vector (8 consecutive h) of token rows g and
+// g + 8 and of expert row g of each column group; its elements 0-3 are that lane's k pairs
+// {2q, 2q+1} and {2q+8, 2q+9} of the first MMA, elements 4-7 those of the second.  The partial
+// tiles are added over the CTA's warps (through shared memory, in warp order) and over the
+// cluster's CTAs: CTA r owns rows r * 16/cl .. of the tile, every CTA sends its partial of those
+// rows into CTA r's shared memory, and CTA r adds them in rank order.  The summation order
+// depends on H alone, so the standalone router and the fused router + top-k give the same bits.
 
-constexpr int RL_TOK = 4, RL_EXP = 8, RL_WARPS = 8;
+constexpr int RT_TOK = 16, RT_EXP = 64, RT_WARPS = 8;
 
-// The block's tile (tokens t0.., experts e0..): thread i * RL_EXP + j (< RL_TOK * RL_EXP)
-// receives output (t0 + i, e0 + j) in `out` and returns true.  Every thread of the block calls it
-// (it synchronises the block).  Shared by the standalone router kernel and the fused router +
-// top-k kernel, so both give the same bits.
-MOE_DEV bool router_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E, int t0,
-                         int e0, float (*s_red)[RL_TOK * RL_EXP], float& out) {
+// Split of h over the cluster: as wide as 8 CTAs while every warp still gets a super-step.
+int router_cluster(int H) {
+  const int ns = (H + 31) / 32;
+  int cl = 8;
+  while (cl > 1 && cl * RT_WARPS > ns) cl >>= 1;
+  return cl;
+}
+
+// D += A * B for one m16n8k16 tile: A row-major 16 x 16 BF16 (a0: row g, k 2q..2q+1; a1: row
+// g + 8; a2, a3: the same at k + 8), B 16 x 8 BF16 (b0: k 2q..2q+1 of column g; b1: k + 8),
+// D 16 x 8 FP32 (d0, d1: row g, columns 2q, 2q + 1; d2, d3: row g + 8).
+MOE_DEV void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct RouterSmem {
+  float red[RT_WARPS][RT_TOK][RT_EXP];  // each warp's partial tile
+  float part[RT_TOK * RT_EXP];          // [sender rank][owned row][expert]: partials of this CTA's rows
+  float rows[RT_TOK][RT_EXP];           // this CTA's finished rows (the top-k's input)
+};
+
+// The logits of the rows CTA `rank` owns (tile rows rank * 16/cl ..), left in s.rows[0 .. 16/cl)
+// and written to `logits`.  Every thread of every CTA of the cluster calls it.
+MOE_DEV void router_cluster_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
+                                 int t0, int e0, int cl, int rank, RouterSmem& s, float* __restrict__ logits) {
+  // this CTA has started: the matching wait below precedes the first store into another CTA
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float v[RL_TOK * RL_EXP];
+  const int g = lane >> 2, q = lane & 3;
+  float acc[RT_EXP / 8][4];
 #pragma unroll
-  for (int i = 0; i < RL_TOK * RL_EXP; ++i) v[i] = 0.f;
-  const int nvec = H / 8;
-  for (int vi = threadIdx.x; vi < nvec; vi += RL_WARPS * 32) {
-    uint4 xv[RL_TOK], wv[RL_EXP];
+  for (int j = 0; j < RT_EXP / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  const int ns = (H + 31) / 32;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int st = rank * RT_WARPS + warp; st < ns; st += cl * RT_WARPS) {
+    const int h = st * 32 + q * 8;
+    const bool hv = h < H;  // H % 8 == 0: a vector is wholly inside or wholly outside
+    const uint4 xa = (hv && t0 + g < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + g) * H + h)) : zero;
+    const uint4 xb =
+        (hv && t0 + g + 8 < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + g + 8) * H + h)) : zero;
+    uint4 wv[RT_EXP / 8];
 #pragma unroll
-    for (int i = 0; i < RL_TOK; ++i)
-      xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + vi) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < RT_EXP / 8; ++j)
+      wv[j] = (hv && e0 + 8 * j + g < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + 8 * j + g) * H + h))
+                                         : zero;
 #pragma unroll
-    for (int j = 0; j < RL_EXP; ++j)
-      wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + j) * H) + vi) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int i = 0; i < RL_TOK; ++i) {
-      const uint32_t xa[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-      for (int j = 0; j < RL_EXP; ++j) {
-        const uint32_t wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-        float a = v[i * RL_EXP + j];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          a = fmaf(bf16_lo(xa[c]), bf16_lo(wa[c]), a);
-          a = fmaf(bf16_hi(xa[c]), bf16_hi(wa[c]), a);
-        }
-        v[i * RL_EXP + j] = a;
-      }
+    for (int j = 0; j < RT_EXP / 8; ++j) {
+      mma_bf16_m16n8k16(acc[j], xa.x, xb.x, xa.y, xb.y, wv[j].x, wv[j].y);
+      mma_bf16_m16n8k16(acc[j], xa.z, xb.z, xa.w, xb.w, wv[j].z, wv[j].w);
     }
   }
-  // reduce-scatter of the 32 sums over the warp: after the step with offset o a lane keeps the
-  // half of its values selected by its lane bit o and adds the partner's copy of that half
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = upper ? v[i] : v[i + o];
-      const float keep = upper ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
+  for (int j = 0; j < RT_EXP / 8; ++j) {
+    *reinterpret_cast<float2*>(&s.red[warp][g][8 * j + 2 * q]) = make_float2(acc[j][0], acc[j][1]);
+    *reinterpret_cast<float2*>(&s.red[warp][g + 8][8 * j + 2 * q]) = make_float2(acc[j][2], acc[j][3]);
   }
-  s_red[warp][lane] = v[0];  // output index lane = i * RL_EXP + j
   __syncthreads();
-  if (threadIdx.x >= RL_TOK * RL_EXP) return false;
-  float a = 0.f;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+  const int rows = RT_TOK / cl;
+  for (int i = threadIdx.x; i < RT_TOK * RT_EXP; i += RT_WARPS * 32) {
+    const int row = i / RT_EXP, col = i % RT_EXP;
+    float v = s.red[0][row][col];
 #pragma unroll
-  for (int ww = 0; ww < RL_WARPS; ++ww) a += s_red[ww][threadIdx.x];
-  out = a;
-  return true;
-}
-
-__global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                                      const uint16_t* __restrict__ w, int T, int H,
-                                                                      int E, float* __restrict__ logits) {
-  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
-  griddep_wait();
-  griddep_launch_dependents();
-  const int t0 = blockIdx.x * RL_TOK;
-  const int e0 = blockIdx.y * RL_EXP;
-  float a;
-  if (router_tile(x, w, T, H, E, t0, e0, s_red, a)) {
-    const int i = threadIdx.x / RL_EXP, j = threadIdx.x % RL_EXP;
-    if (t0 + i < T && e0 + j < E) logits[(size_t)(t0 + i) * E + e0 + j] = a;
+    for (int ww = 1; ww < RT_WARPS; ++ww) v += s.red[ww][row][col];
+    st_shared_cluster_f32(smem_u32(&s.part[(rank * rows + row % rows) * RT_EXP + col]), row / rows, v);
   }
-}
-
-int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st) {
-  dim3 grid((T + RL_TOK - 1) / RL_TOK, (E + RL_EXP - 1) / RL_EXP);
-  return launch_pdl(router_logits_kernel, grid, dim3(RL_WARPS * 32), 0, st, x, w, T, H, E, logits);
+  cluster_sync_all();  // every CTA's partials of the rows it owns are in its shared memory
+  for (int i = threadIdx.x; i < rows * RT_EXP; i += RT_WARPS * 32) {
+    const int lr = i / RT_EXP, col = i % RT_EXP;
+    float v = s.part[lr * RT_EXP + col];
+    for (int r = 1; r < cl; ++r) v += s.part[(r * rows + lr) * RT_EXP + col];
+    s.rows[lr][col] = v;
+    const int t = t0 + rank * rows + lr, e = e0 + col;
+    if (t < T && e < E) logits[(size_t)t * E + e] = v;
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -108,7 +120,13 @@ int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int
 
 constexpr int TOPK_WARPS = 8;
 
-MOE_DEV bool key_better(float ka, int ea, float kb, int eb) { return ka > kb || (ka == kb && ea < eb); }
+// Order-preserving code of a selection key: a larger key gets a larger code, +0 and -0 the same
+// one, and every key (-inf included) a code above 0, which marks "no candidate".
+MOE_DEV uint32_t key_code(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // One warp routes one row: top-k of (logit + bias) with ties to the lower expert index, weights
 // from the unbiased logits (softmax over the k picks, or over all experts).  `lrow` may point to
@@ -131,30 +149,27 @@ MOE_DEV void topk_row(const float* lrow, const float* __restrict__ bias, int E, 
     }
   }
   if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_error(err, MOE_DEVERR_NAN_LOGIT);
-  uint32_t taken = 0;
+  // selection s: the largest remaining key, ties to the lower expert.  A lane's candidate is its
+  // best remaining code (strict >: the lower j, i.e. the lower expert, on ties); the warp takes
+  // the largest code, then the lowest expert among the lanes holding it.
+  uint32_t code[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) code[j] = lane + 32 * j < E ? key_code(key[j]) : 0u;
   int my_id = -1;
   for (int s = 0; s < k; ++s) {
-    float bk = -INFINITY;
-    int be = 0x7fffffff;
+    uint32_t bc = 0u, be = 0x7fffffffu;
 #pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && key_better(key[j], e, bk, be)) {
-        bk = key[j];
-        be = e;
+    for (int j = 0; j < NPL; ++j)
+      if (code[j] > bc) {
+        bc = code[j];
+        be = lane + 32 * j;
       }
-    }
+    const uint32_t mc = __reduce_max_sync(0xffffffffu, bc);
+    const int pick = (int)__reduce_min_sync(0xffffffffu, bc == mc ? be : 0x7fffffffu);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (key_better(ok, oe, bk, be)) {
-        bk = ok;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == s) my_id = be;
+    for (int j = 0; j < NPL; ++j)
+      if (pick == lane + 32 * j) code[j] = 0u;
+    if (lane == s) my_id = pick;
   }
   // routing weights from the unbiased logits
   const bool mine = lane < k;
@@ -220,49 +235,52 @@ int route_topk_launch(const float* logits, const float* bias, int T, int E, int 
 }
 
 // ------------------------------------------------------------------------------------------------
-// router logits + top-k in one launch (the forward's routing when it owns the router GEMM and
-// E <= 64): a cluster of ceil(E / 8) CTAs takes 4 rows; CTA r computes the 4 x 8 logit tile of
-// experts 8r.. exactly as the standalone router kernel does, writes it to global memory and into
-// the shared memory of CTA 0 of the cluster; after the cluster barrier, warps 0..3 of CTA 0 route
-// one row each with the standalone top-k routine.  Same bits as the two separate launches, one
-// launch and one HBM round trip of the logits fewer.
+// router kernels.  TOPK = false: the standalone router (any E, 64-expert tiles along grid z).
+// TOPK = true: router logits + top-k in one launch (the forward's routing when it owns the router
+// GEMM and E <= 64): after the cluster reduction each CTA routes the rows it owns, one warp per
+// row, with the standalone top-k routine.  Same bits as the two separate launches, one launch and
+// one HBM round trip of the logits fewer.
 
-template <int NPL>
-__global__ void __launch_bounds__(RL_WARPS * 32)
-    router_topk_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
-                       const float* __restrict__ bias, int k, int renormalize, float routed_scale,
-                       float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int* err) {
-  __shared__ float s_red[RL_WARPS][RL_TOK * RL_EXP];
-  __shared__ float s_log[RL_TOK][32 * NPL];  // CTA 0's copy receives every CTA's tile
+template <bool TOPK, int NPL>
+__global__ void __launch_bounds__(RT_WARPS * 32)
+    router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
+                  const float* __restrict__ bias, int k, int renormalize, float routed_scale,
+                  float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int* err) {
+  __shared__ __align__(16) RouterSmem s;
   griddep_wait();
   griddep_launch_dependents();
-  const int t0 = blockIdx.y * RL_TOK;
-  const int e0 = blockIdx.x * RL_EXP;  // blockIdx.x == rank in the cluster
-  float a;
-  if (router_tile(x, w, T, H, E, t0, e0, s_red, a)) {
-    const int i = threadIdx.x / RL_EXP, e = e0 + threadIdx.x % RL_EXP;
-    if (e < E) {
-      if (t0 + i < T) logits[(size_t)(t0 + i) * E + e] = a;
-      st_shared_cluster_f32(smem_u32(&s_log[i][e]), 0, a);
+  const int cl = gridDim.x, rank = blockIdx.x;  // the cluster spans grid x
+  const int t0 = blockIdx.y * RT_TOK, e0 = blockIdx.z * RT_EXP;
+  router_cluster_tile(x, w, T, H, E, t0, e0, cl, rank, s, logits);
+  if constexpr (TOPK) {
+    __syncthreads();
+    const int rows = RT_TOK / cl;
+    for (int lr = threadIdx.x >> 5; lr < rows; lr += RT_WARPS) {
+      const int t = t0 + rank * rows + lr;
+      if (t < T)
+        topk_row<NPL>(s.rows[lr], bias, E, k, renormalize, routed_scale, ids + (size_t)t * k, wts + (size_t)t * k,
+                      err);
     }
   }
-  cluster_sync_all();  // the cluster's tiles are in CTA 0's shared memory
-  const int warp = threadIdx.x >> 5;
-  if (cluster_ctarank() == 0 && warp < RL_TOK && t0 + warp < T)
-    topk_row<NPL>(s_log[warp], bias, E, k, renormalize, routed_scale, ids + (size_t)(t0 + warp) * k,
-                  wts + (size_t)(t0 + warp) * k, err);
+}
+
+int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st) {
+  const int cl = router_cluster(H);
+  const dim3 grid(cl, (T + RT_TOK - 1) / RT_TOK, (E + RT_EXP - 1) / RT_EXP);
+  return launch_pdl_cluster(router_kernel<false, 1>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, nullptr, 0,
+                            0, 0.f, logits, nullptr, nullptr, nullptr);
 }
 
 int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, const float* bias, int k,
                        int renormalize, float scale, float* logits, int32_t* ids, float* wts, int* err,
                        cudaStream_t st) {
   if (E > kRouterTopkMaxE) return MOE_ERR_UNSUPPORTED_SHAPE;
-  const int groups = (E + RL_EXP - 1) / RL_EXP;  // cluster size, <= 8
-  const dim3 grid(groups, (T + RL_TOK - 1) / RL_TOK);
+  const int cl = router_cluster(H);
+  const dim3 grid(cl, (T + RT_TOK - 1) / RT_TOK, 1);
   if (E <= 32)
-    return launch_pdl_cluster(router_topk_kernel<1>, grid, dim3(RL_WARPS * 32), 0, st, groups, x, w, T, H, E, bias,
-                              k, renormalize, scale, logits, ids, wts, err);
-  return launch_pdl_cluster(router_topk_kernel<2>, grid, dim3(RL_WARPS * 32), 0, st, groups, x, w, T, H, E, bias, k,
+    return launch_pdl_cluster(router_kernel<true, 1>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, bias, k,
+                              renormalize, scale, logits, ids, wts, err);
+  return launch_pdl_cluster(router_kernel<true, 2>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, bias, k,
                             renormalize, scale, logits, ids, wts, err);
 }
 

@@ -61,6 +61,17 @@ def test_router_logits_c1_shapes():
     assert nerr(got, ref) < 1e-5
 
 
+@pytest.mark.parametrize("T,H,E", [(1, 8, 1), (37, 512, 5), (17, 264, 130), (300, 2048, 160), (33, 5120, 64)])
+def test_router_logits_ragged_shapes(T, H, E):
+    """Token counts off the 16-row tile, E off the 8- and 64-expert groups, H off the 32-element
+    step and split 1, 2 or 8 ways over the cluster."""
+    g = np.random.default_rng(T * H + E)
+    x = S.bf16_bits_from_f32(g.standard_normal((T, H)).astype(np.float32))
+    w = S.bf16_bits_from_f32(g.normal(0.0, 0.02, (E, H)).astype(np.float32))
+    got = moe.moe_router_logits(bf16_dev(x), bf16_dev(w)).cpu().numpy()
+    assert nerr(got, O.router_logits(x, w)) < 1e-5
+
+
 @pytest.mark.parametrize("T,E,k,bias,renorm", [(300, 160, 8, False, 1), (257, 64, 8, True, 1),
                                                (33, 16, 8, False, 0), (5, 1000, 32, True, 1), (40, 9, 9, False, 1)])
 def test_route_topk_bit_exact(T, E, k, bias, renorm):

@@ -291,8 +291,9 @@ int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E
 //   scatter: one block per segment; the sorted position of a slot is
 //              (slots of all buckets < b) + (slots of bucket b in earlier segments)
 //              + (slots of bucket b earlier in this segment),
-//            the last term from __match_any_sync ranks inside 32-slot chunks plus per-warp running
-//            counts, which keeps flat slot order (a stable sort).  Block 0 writes expert_offsets.
+//            the last term from the lanes with the same bucket (ballots over the bucket's bits)
+//            inside 32-slot chunks plus per-warp running counts, which keeps flat slot order (a
+//            stable sort).  Block 0 writes expert_offsets.
 
 constexpr int SORT_SEG = 2048;
 constexpr int SORT_THREADS = 256;
@@ -307,6 +308,19 @@ int sort_segments(int R, int E) {
 size_t sort_scratch_bytes(int R, int E) { return (size_t)(E + 1) * sort_segments(R, E) * sizeof(int32_t); }
 
 MOE_DEV int bucket_of(int id, int E) { return (id >= 0 && id < E) ? id : E; }
+
+// Lanes of the warp whose key equals this lane's (0 <= key < 2^nbits): the AND over the key's
+// bits of the ballot of that bit (or of its complement where the bit is clear).  nbits
+// independent ballots take the place of a warp match, which is slow.
+MOE_DEV uint32_t same_key_lanes(int key, int nbits) {
+  uint32_t m = 0xffffffffu;
+  for (int i = 0; i < nbits; ++i) {
+    const bool bit = (key >> i) & 1;
+    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
 
 __global__ void __launch_bounds__(SORT_THREADS)
     sort_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int S, int32_t* __restrict__ cnt, int* err) {
@@ -392,12 +406,13 @@ __global__ void __launch_bounds__(SORT_THREADS)
 
   // (2) stable ranks inside the segment
   const uint32_t lt = (1u << lane) - 1u;
+  const int nbits = 32 - __clz(E + 1);  // keys b + 1 lie in [0, E + 1]
   int16_t* wc = s_wcnt + warp * NB;
 #pragma unroll
   for (int c = 0; c < SORT_PER_WARP; c += 32) {
     const int li = warp * SORT_PER_WARP + c + lane;  // slot index inside the segment
     const int b = bk[c / 32];
-    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    const uint32_t peers = same_key_lanes(b + 1, nbits);  // b = -1 (no slot) -> key 0
     int local = 0;
     if (b >= 0) local = wc[b] + __popc(peers & lt);
     __syncwarp();
@@ -459,12 +474,13 @@ __global__ void __launch_bounds__(SORT_THREADS)
   if (__syncthreads_or(bad) && tid == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
   // stable ranks inside each warp's run of slots, per-warp bucket counts
   const uint32_t lt = (1u << lane) - 1u;
+  const int nbits = 32 - __clz(E + 1);  // keys b + 1 lie in [0, E + 1]
   int16_t* wc = s_wcnt + warp * NB;
 #pragma unroll
   for (int c = 0; c < SORT_PER_WARP / 32; ++c) {
     const int li = warp * SORT_PER_WARP + c * 32 + lane;
     const int b = bk[c];
-    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    const uint32_t peers = same_key_lanes(b + 1, nbits);  // b = -1 (no slot) -> key 0
     int local = 0;
     if (b >= 0) local = wc[b] + __popc(peers & lt);
     __syncwarp();
@@ -506,12 +522,16 @@ __global__ void __launch_bounds__(SORT_THREADS)
     }
   }
   __syncthreads();
-  for (int i = tid; i < R; i += SORT_THREADS) {
-    const int b = s_bkt[i];
-    const int p = s_base[b] + s_wcnt[(i / SORT_PER_WARP) * NB + b] + s_lpos[i];
-    sorted_token_ids[p] = i / k;
-    sorted_expert_ids[p] = b < E ? b : -1;
-    token_to_perm[i] = b < E ? p : -1;
+#pragma unroll
+  for (int c = 0; c < SORT_SEG / SORT_THREADS; ++c) {
+    const int i = tid + c * SORT_THREADS;
+    if (i < R) {
+      const int b = s_bkt[i];
+      const int p = s_base[b] + s_wcnt[(i / SORT_PER_WARP) * NB + b] + s_lpos[i];
+      sorted_token_ids[p] = i / k;
+      sorted_expert_ids[p] = b < E ? b : -1;
+      token_to_perm[i] = b < E ? p : -1;
+    }
   }
 }
 

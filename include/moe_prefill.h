@@ -317,19 +317,22 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  * indexed combine.  No host round trip (the pages read expert_offsets back once; here the
  * GEMMs schedule their tiles from expert_offsets on the device), so the call can be captured
  * in a CUDA graph.
- *   x          device BF16 [T, H]
+ *   x          BF16 [T, H], device memory or host memory the device can read (page-locked, or
+ *              any host memory where the device has pageable memory access): a host x is staged
+ *              into the workspace's x_stage by the router kernel as it reads it (without a router,
+ *              by one copy on `stream`), and the expert GEMMs read the staged rows
  *   w_router   device BF16 [E, H] or NULL
- *   logits_in  device FP32 [T, E] or NULL  (exactly one of w_router / logits_in)
+ *   logits_in  FP32 [T, E] or NULL (exactly one of w_router / logits_in); device memory or host
+ *              memory the device can read (the top-k reads it in place)
  *   router_bias device FP32 [E] or NULL (selection only)
  *   w_gate_up  table with E = cfg E, N = 2I, K = H;  w_down: E, N = H, K = I
  *   ws, ws_bytes device workspace >= moe_workspace_bytes(cfg, T), 256-byte aligned (G takes
  *              space only with MOE_FWD_SEPARATE_SWIGLU).  Its
  *              contents after the call: logits, ids, wts, the sort arrays, G, act, Y, at the
  *              offsets moe_workspace_layout reports.
- *   out        BF16 [T, H] in memory the device can store to: device memory, or page-locked
- *              host memory (the combine then writes the result straight to the host; no copy
- *              follows).  Other pointers: MOE_ERR_INVALID_ARG, unless the device has pageable
- *              memory access.
+ *   out        BF16 [T, H] in memory the device can store to: device memory, or host memory
+ *              as for x (the combine then writes the result straight to the host; no copy
+ *              follows).  An x, logits_in or out the device cannot reach: MOE_ERR_INVALID_ARG.
  *   shared_out device BF16 [T, H] or NULL: the shared expert's output, added in the combine
  *              (moe_shared_expert_forward)
  *   shared_ready NULL, or a cudaEvent_t (as void*) the stream waits for right before the
@@ -359,10 +362,11 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
 /* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection).
  * `ready`: INT32 [E + 1], per-expert counters through which the down GEMM starts on an expert as
  * soon as the gate/up GEMM has stored its activation rows, and the down GEMM's dynamic tile
- * counter (cleared by the sort on every call). */
+ * counter (cleared by the sort on every call).  `x_stage`: BF16 [T, H], the device copy of an x
+ * passed in host memory (unused when x is device memory). */
 typedef struct {
   size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, ready,
-      G, act, Y, total;
+      G, act, Y, x_stage, total;
 } moe_workspace_layout_t;
 int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_workspace_layout_t* layout);
 

@@ -59,7 +59,7 @@ class MoePrefillConfig(ctypes.Structure):
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "ids", "wts", "sorted_token_ids", "sorted_expert_ids",
                                                "expert_offsets", "token_to_perm", "sort_scratch", "ready", "G", "act", "Y",
-                                               "total")]
+                                               "x_stage", "total")]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -378,13 +378,19 @@ def moe_prefill_forward(cfg: MoePrefillConfig, x: torch.Tensor, w_gate_up: Exper
                         out: Optional[torch.Tensor] = None, stage_events: Optional[Sequence] = None,
                         stream=None, shared_out: Optional[torch.Tensor] = None, shared_ready=None) -> torch.Tensor:
     """`shared_out`: the shared expert's BF16 [T, H] output, added in the combine; `shared_ready`:
-    a torch.cuda.Event the stream waits for before the combine (shared_out made on another stream)."""
-    _need(x, torch.bfloat16, "x")
+    a torch.cuda.Event the stream waits for before the combine (shared_out made on another stream).
+    `x`, `logits` and `out` may also be (pinned) host tensors: the library checks that the device
+    can reach them, stages a host x into the workspace on the device, reads host logits in place
+    and stores into a host out directly."""
+    for t, n, dt in ((x, "x", torch.bfloat16), (logits, "logits", torch.float32), (out, "out", torch.bfloat16)):
+        if t is not None and (t.dtype != dt or not t.is_contiguous() or t.device.type not in ("cuda", "cpu")):
+            raise ValueError(f"{n}: need a contiguous {dt} tensor (CUDA or host), got {t.dtype} on {t.device}")
     if shared_out is not None:
         _need(shared_out, torch.bfloat16, "shared_out")
     T = x.shape[0]
     if out is None:
-        out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=x.device)
+        dev = x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
     ev = None
     if stage_events is not None:
         ev = (_P * MOE_FWD_NUM_EVENTS)(*[e.cuda_event for e in stage_events])

@@ -68,26 +68,31 @@ int ensure_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// True when kernels on the current device may store through p: device or managed memory,
-// page-locked host memory (unified addressing maps it at the same address), or any host memory
-// on a device with pageable memory access (a coherent CPU-GPU node).  The pointer query is not a
-// stream operation, so it runs in relaxed capture mode while a CUDA graph is being captured.
-bool device_accessible(const void* p) {
+// Where p points, for the current device: kMemDevice (device or managed memory), kMemHost (host
+// memory kernels can read and write: page-locked host memory, which unified addressing maps at
+// the same address, or any host memory on a device with pageable memory access, a coherent
+// CPU-GPU node), or kMemNone.  The pointer query is not a stream operation, so it runs in relaxed
+// capture mode while a CUDA graph is being captured.
+enum MemKind { kMemNone, kMemDevice, kMemHost };
+
+MemKind memory_kind(const void* p) {
   cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
-  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return false;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return kMemNone;
   cudaPointerAttributes a{};
   const cudaError_t e = cudaPointerGetAttributes(&a, p);
   cudaThreadExchangeStreamCaptureMode(&mode);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return kMemNone;
   }
-  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
-  if (a.type == cudaMemoryTypeHost) return a.devicePointer == p;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return kMemDevice;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer == p ? kMemHost : kMemNone;
   int pageable = 0;
   const int d = current_device();
   return d >= 0 && cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, d) == cudaSuccess &&
-         pageable != 0;
+                 pageable != 0
+             ? kMemHost
+             : kMemNone;
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -511,6 +516,7 @@ int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspac
   L->G = take((c->flags & MOE_FWD_SEPARATE_SWIGLU) ? R * 2 * I * 2 : 0);
   L->act = take(R * I * 2);
   L->Y = take(R * H * 2);
+  L->x_stage = take(T * H * 2);
   L->total = o;
   return MOE_OK;
 }
@@ -541,7 +547,12 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   rc = ensure_device();
   if (rc != MOE_OK) return rc;
   if (current_device() != w_gate_up->device || current_device() != w_down->device) return MOE_ERR_INVALID_ARG;
-  if (!device_accessible(out)) return MOE_ERR_INVALID_ARG;
+  // x and logits_in may be host memory the device can read, out host memory it can write: the
+  // router kernel stages a host x into the workspace as it reads it (without a router, one
+  // copy does), the top-k reads host logits directly, the combine stores into host memory
+  const MemKind x_kind = memory_kind(x);
+  if (x_kind == kMemNone || memory_kind(out) == kMemNone) return MOE_ERR_INVALID_ARG;
+  if (logits_in && memory_kind(logits_in) == kMemNone) return MOE_ERR_INVALID_ARG;
 
   cudaStream_t st = as_stream(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -556,6 +567,8 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   uint16_t* G = reinterpret_cast<uint16_t*>(base + L.G);
   uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
   uint16_t* Y = reinterpret_cast<uint16_t*>(base + L.Y);
+  uint16_t* x_stage = x_kind == kMemHost ? reinterpret_cast<uint16_t*>(base + L.x_stage) : nullptr;
+  const uint16_t* xg = x_stage ? x_stage : x;  // the rows the expert GEMMs read
   const int R = T * k;
   int* err = device_error_word();
   // inside a stream capture the events become timestamp nodes of the graph (external records)
@@ -568,17 +581,20 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   };
 
   ev(0);
+  if (x_stage && !w_router &&
+      cudaMemcpyAsync(x_stage, x, (size_t)T * H * 2, cudaMemcpyDefault, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (w_router && E <= kRouterTopkMaxE) {
     // router GEMM and top-k in one launch (stage 1 -> 2 is empty): same results as the two
     // standalone entry points
     rc = router_topk_launch(x, w_router, T, H, E, router_bias, k, cfg->renormalize, cfg->routed_scale, logits, ids,
-                            wts, err, st);
+                            wts, err, st, x_stage);
     if (rc != MOE_OK) return rc;
     ev(1);
   } else {
     const float* lg = logits_in;
     if (w_router) {
-      if ((rc = router_logits_launch(x, w_router, T, H, E, logits, st)) != MOE_OK) return rc;
+      if ((rc = router_logits_launch(x, w_router, T, H, E, logits, st, x_stage)) != MOE_OK) return rc;
       lg = logits;
     }
     ev(1);
@@ -597,16 +613,16 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   ev(3);
   // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
   if (small) {
-    rc = gemv_checked(x, T, H, sti, w_gate_up, off, R, act, I, I, cfg->swiglu_limit, st);
+    rc = gemv_checked(xg, T, H, sti, w_gate_up, off, R, act, I, I, cfg->swiglu_limit, st);
     if (rc != MOE_OK) return rc;
     ev(4);
   } else if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
-    if ((rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+    if ((rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
   } else {
     // one producer CTA tile per 128 activation columns (a gate block and its up block)
-    rc = gemm_checked(x, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit, ready,
+    rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit, ready,
                       nullptr, I / 128);
     if (rc != MOE_OK) return rc;
     ev(4);

@@ -111,13 +111,16 @@ int shared_expert_launch(const uint16_t* x, int T, int H, int I, const uint16_t*
                          const uint16_t* w_down, float limit, void* ws, uint16_t* shared_out, cudaStream_t st);
 
 // SIMT kernels (small_kernels.cu)
-int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st);
+// Router logits (tensor-core MMAs, h split over a cluster of up to 8 CTAs per 16 rows).  x_copy:
+// NULL, or a device BF16 [T, H] buffer that receives x as the kernel reads it (x in host memory).
+int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st,
+                         uint16_t* x_copy = nullptr);
 // router logits + top-k in one launch (same results as router_logits_launch + route_topk_launch)
-// when E <= 64 (one cluster of E/8 CTAs per 4 rows); MOE_ERR_UNSUPPORTED_SHAPE otherwise
+// when E <= 64; MOE_ERR_UNSUPPORTED_SHAPE otherwise
 constexpr int kRouterTopkMaxE = 64;
 int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, const float* bias, int k,
                        int renormalize, float scale, float* logits, int32_t* ids, float* wts, int* err,
-                       cudaStream_t st);
+                       cudaStream_t st, uint16_t* x_copy = nullptr);
 int route_topk_launch(const float* logits, const float* bias, int T, int E, int k, int renormalize, float scale,
                       int32_t* ids, float* wts, int* err, cudaStream_t st);
 int sort_segments(int R, int E);

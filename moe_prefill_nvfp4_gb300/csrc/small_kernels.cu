@@ -60,9 +60,12 @@ struct RouterSmem {
 };
 
 // The logits of the rows CTA `rank` owns (tile rows rank * 16/cl ..), left in s.rows[0 .. 16/cl)
-// and written to `logits`.  Every thread of every CTA of the cluster calls it.
+// and written to `logits`.  Every thread of every CTA of the cluster calls it.  x_copy (NULL, or
+// device BF16 [T, H]): the first 64-expert tile's clusters store every x vector they load there
+// (each vector of x is loaded by exactly one lane of them), staging an x held in host memory.
 MOE_DEV void router_cluster_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
-                                 int t0, int e0, int cl, int rank, RouterSmem& s, float* __restrict__ logits) {
+                                 int t0, int e0, int cl, int rank, RouterSmem& s, float* __restrict__ logits,
+                                 uint16_t* __restrict__ x_copy) {
   // this CTA has started: the matching wait below precedes the first store into another CTA
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +86,10 @@ MOE_DEV void router_cluster_tile(const uint16_t* __restrict__ x, const uint16_t*
     for (int j = 0; j < RT_EXP / 8; ++j)
       wv[j] = (hv && e0 + 8 * j + g < E) ? __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + 8 * j + g) * H + h))
                                          : zero;
+    if (x_copy != nullptr && e0 == 0 && hv) {
+      if (t0 + g < T) *reinterpret_cast<uint4*>(x_copy + (size_t)(t0 + g) * H + h) = xa;
+      if (t0 + g + 8 < T) *reinterpret_cast<uint4*>(x_copy + (size_t)(t0 + g + 8) * H + h) = xb;
+    }
 #pragma unroll
     for (int j = 0; j < RT_EXP / 8; ++j) {
       mma_bf16_m16n8k16(acc[j], xa.x, xb.x, xa.y, xb.y, wv[j].x, wv[j].y);
@@ -245,13 +252,14 @@ template <bool TOPK, int NPL>
 __global__ void __launch_bounds__(RT_WARPS * 32)
     router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int T, int H, int E,
                   const float* __restrict__ bias, int k, int renormalize, float routed_scale,
-                  float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int* err) {
+                  float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts, int* err,
+                  uint16_t* __restrict__ x_copy) {
   __shared__ __align__(16) RouterSmem s;
   griddep_wait();
   griddep_launch_dependents();
   const int cl = gridDim.x, rank = blockIdx.x;  // the cluster spans grid x
   const int t0 = blockIdx.y * RT_TOK, e0 = blockIdx.z * RT_EXP;
-  router_cluster_tile(x, w, T, H, E, t0, e0, cl, rank, s, logits);
+  router_cluster_tile(x, w, T, H, E, t0, e0, cl, rank, s, logits, x_copy);
   if constexpr (TOPK) {
     __syncthreads();
     const int rows = RT_TOK / cl;
@@ -264,24 +272,25 @@ __global__ void __launch_bounds__(RT_WARPS * 32)
   }
 }
 
-int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st) {
+int router_logits_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits, cudaStream_t st,
+                         uint16_t* x_copy) {
   const int cl = router_cluster(H);
   const dim3 grid(cl, (T + RT_TOK - 1) / RT_TOK, (E + RT_EXP - 1) / RT_EXP);
   return launch_pdl_cluster(router_kernel<false, 1>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, nullptr, 0,
-                            0, 0.f, logits, nullptr, nullptr, nullptr);
+                            0, 0.f, logits, nullptr, nullptr, nullptr, x_copy);
 }
 
 int router_topk_launch(const uint16_t* x, const uint16_t* w, int T, int H, int E, const float* bias, int k,
                        int renormalize, float scale, float* logits, int32_t* ids, float* wts, int* err,
-                       cudaStream_t st) {
+                       cudaStream_t st, uint16_t* x_copy) {
   if (E > kRouterTopkMaxE) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int cl = router_cluster(H);
   const dim3 grid(cl, (T + RT_TOK - 1) / RT_TOK, 1);
   if (E <= 32)
     return launch_pdl_cluster(router_kernel<true, 1>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, bias, k,
-                              renormalize, scale, logits, ids, wts, err);
+                              renormalize, scale, logits, ids, wts, err, x_copy);
   return launch_pdl_cluster(router_kernel<true, 2>, grid, dim3(RT_WARPS * 32), 0, st, cl, x, w, T, H, E, bias, k,
-                            renormalize, scale, logits, ids, wts, err);
+                            renormalize, scale, logits, ids, wts, err, x_copy);
 }
 
 // ------------------------------------------------------------------------------------------------

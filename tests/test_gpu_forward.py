@@ -244,24 +244,38 @@ def test_forward_graph_capture_replay():
     db.close()
 
 
-def test_output_into_pinned_host_memory():
-    """out may be page-locked host memory: the combine stores the result there directly, eagerly
-    and inside a captured graph, bit-identical to the device-memory result."""
-    c = S.make_block_case(T=96, H=512, I=256, E=12, k=4, routing="biased", seed=36)
+@pytest.mark.parametrize("routing,E", [("biased", 12), ("router", 12), ("router", 80)],
+                         ids=["host-logits", "router-fused-topk", "router-e80"])
+def test_host_memory_inputs_and_output(routing, E):
+    """x, logits and out may be page-locked host memory: a host x is staged into the workspace
+    (by the router kernel, or by one copy without a router), host logits are read in place, the
+    combine stores into the host out.  Eagerly and inside a captured graph the result equals the
+    device-memory run bit for bit."""
+    c = S.make_block_case(T=96, H=512, I=256, E=E, k=4, routing=routing, seed=36)
     db = DeviceBlock(c)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         db.forward(stream=s)
     torch.cuda.synchronize()
     ref = db.out.cpu()
+    x_host = db.x.cpu().pin_memory()
+    lg_host = db.logits.cpu().pin_memory() if db.logits is not None else None
     host = torch.zeros(c.T, c.H, dtype=torch.bfloat16).pin_memory()
-    moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, logits=db.logits, out=host, stream=s)
+    db.ws.zero_()
+
+    def run():
+        moe.moe_prefill_forward(db.cfg, x_host, db.gu.table, db.dn.table, db.ws, w_router=db.router_w,
+                                logits=lg_host, out=host, stream=s)
+
+    run()
     s.synchronize()
     assert torch.equal(host.view(torch.int16), ref.view(torch.int16))
+    staged = db.ws_view("x_stage", torch.bfloat16, (c.T, c.H))
+    assert torch.equal(staged.cpu().view(torch.int16), x_host.view(torch.int16))
     host.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        moe.moe_prefill_forward(db.cfg, db.x, db.gu.table, db.dn.table, db.ws, logits=db.logits, out=host, stream=s)
+        run()
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(host.view(torch.int16), ref.view(torch.int16))

@@ -35,7 +35,7 @@ namespace moe {
 constexpr int RT_TOK = 16, RT_EXP = 64, RT_WARPS = 8;
 
 // Split of h over the cluster: as wide as 8 CTAs while every warp still gets a super-step.
-int router_cluster(int H) {
+static int router_cluster(int H) {
   const int ns = (H + 31) / 32;
   int cl = 8;
   while (cl > 1 && cl * RT_WARPS > ns) cl >>= 1;

@@ -1,14 +1,24 @@
 """Benchmark of the routed-MoE NVFP4 (W4A16) prefill path on GB300 through the C ABI.
 
-One step = one ``moe_prefill_forward`` over one prefill chunk (router GEMM, top-k, expert
-sort, grouped gate/up GEMM, SwiGLU, grouped down GEMM, combine), inputs already resident in
-HBM.  Default workload: the full routed-MoE block on one 256-row chunk (hidden 2048,
-moe_intermediate 768, 64 experts, top-8, BF16 router [64, 2048]).  L2 is flushed between
-timed steps by writing a 256 MiB buffer outside the timed events.
+One step = one ``moe_prefill_forward`` over one prefill chunk (routing, expert sort, grouped
+gate/up GEMM with the fused SwiGLU, grouped down GEMM, combine), inputs already resident in
+HBM.  The headline workload is the largest single-GPU configuration: Zipf(1.2)-skewed routing
+at GLM shapes (hidden 5120, moe_intermediate 1536, 160 experts, top-8), one 8192-row chunk.
+L2 is flushed between timed steps by writing a 256 MiB buffer outside the timed events.
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead, on a
-bounded sample of the same workload.  Multi-GPU (torchrun): independent replicas, one chunk
-per rank per step ("replicas only": the path has no exchange step on one node of this design).
+The same JSON line also carries, as extra keys, the other workloads of the path:
+* ``workloads.c1`` / ``workloads.c2``: the full routed-MoE block on a 256-row chunk (hidden
+  2048, 64 experts, router GEMM) and the balanced 2048-row GLM chunk, each with its own
+  roofline, CPU-oracle baseline and end-to-end number;
+* ``c0``: the single grouped GEMM (64 tokens, 16 experts, N 256, K 512), whose time is launch
+  latency, reported as such;
+* ``c4_sweep``: the row-count sweep at GLM shapes (8 ... 16384 rows) with tokens/s, TFLOP/s,
+  the binding roofline fraction of each grouped GEMM, and the weight bytes read per launch
+  against the once-per-expert minimum.
+
+Prints ONE JSON line.  ``--impl reference`` times the CPU oracle instead, on a bounded sample
+of the same workload.  One GPU only: the grouped GEMM's activation loads multicast within a
+thread-block cluster of this GPU's memory, so ``--gpus`` > 1 is refused.
 """
 
 from __future__ import annotations
@@ -32,10 +42,14 @@ WORKLOAD_DESC = {
           "BF16 router GEMM, NVFP4 gate/up [1536,2048] and down [2048,768] per expert",
     "c2": "GLM-scale routed MoE, 2048-row prefill chunk: hidden 5120, moe_intermediate 1536, 160 experts, top-8, "
           "synthetic logits N(0,1)+bias N(0,0.1)",
-    "c3": "Zipf(1.2) skewed routing at GLM shapes, 8192 rows, 16 experts never chosen",
-    "c1s": "the 256-row chunk of c1 plus the shared expert (dense BF16 SwiGLU MLP, intermediate 768, cuBLAS "
-           "GEMMs) on a second stream, joined in the combine",
+    "c3": "Zipf(1.2) skewed routing at GLM shapes (hidden 5120, moe_intermediate 1536, 160 experts, top-8), "
+          "8192-row prefill chunk, 16 experts never chosen",
+    "c1s": "the 256-row chunk of c1 plus the shared expert (dense BF16 SwiGLU MLP, intermediate 768) on a second "
+           "stream, joined in the combine",
 }
+C0_DESC = "single grouped W4A16 GEMM: 64 tokens x top-8 of 16 experts (512 sorted rows), N 256, K 512, gathered rows"
+C4_DESC = "row-count sweep at GLM shapes (hidden 5120, moe_intermediate 1536, 160 experts, top-8), balanced routing"
+HEADLINE = "c3"
 METRIC = "routed-MoE prefill tokens/s/layer"
 
 
@@ -108,13 +122,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ---------------------------------------------------------------------------------------------- GPU
+# ------------------------------------------------------------------------------------ arithmetic
 
 
-def build_case(name: str):
-    from synth import inputs as S
-
-    return S.workload(name)
+def weight_bytes_min(E_touched: int, N: int, K: int) -> int:
+    """Each touched expert's packed weights, E4M3 scales and FP32 scale2, read once."""
+    return E_touched * (N * K // 2 + N * K // 16 + 4)
 
 
 def gemm_bytes(case, off: np.ndarray, proj: str) -> int:
@@ -128,8 +141,28 @@ def gemm_bytes(case, off: np.ndarray, proj: str) -> int:
         N, K, a_bytes, c_bytes = 2 * case.I, case.H, case.T * case.H * 2, R * case.I * 2
     else:
         N, K, a_bytes, c_bytes = case.H, case.I, R * case.I * 2, R * case.H * 2
-    w = touched * (N * K // 2 + N * K // 16 + 4)
-    return w + a_bytes + c_bytes
+    return weight_bytes_min(touched, N, K) + a_bytes + c_bytes
+
+
+def gemm_flops(case, proj: str) -> int:
+    R = case.T * case.k
+    return 2 * R * 2 * case.I * case.H if proj == "gate_up" else 2 * R * case.H * case.I
+
+
+def roofline_entry(name: str, nbytes: int, flops: int, dur_s: float, peaks: dict, src: str, traffic) -> dict:
+    """Binding roofline of one launch: HBM when bytes/peak_HBM >= flops/peak_TC, else tensor."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = nbytes / dur_s / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic, "algorithmic_bytes": int(nbytes),
+                "algorithmic_flops": int(flops), "us": round(dur_s * 1e6, 2), "peak_source": src}
+    ach = flops / dur_s / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
+            "algorithmic_bytes": int(nbytes), "algorithmic_flops": int(flops), "us": round(dur_s * 1e6, 2),
+            "peak_source": src}
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -173,9 +206,10 @@ def gemm_sources_digest() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str, launch: str):
-    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
-    kernel's sources changed since those counters were taken (or the workload was not captured)."""
+def measured_traffic(workload: str, launch: str, kind: str = "total"):
+    """DRAM bytes per launch from the committed ncu summary (read + write for ``total``, read
+    only for ``read``), or None when the kernel's sources changed since those counters were
+    taken or the workload was not captured."""
     digest = gemm_sources_digest()
     path = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.txt")
     if not os.path.exists(path):
@@ -184,219 +218,383 @@ def measured_traffic(workload: str, launch: str):
         for line in f:
             p = line.split()
             if len(p) == 5 and not line.startswith("#") and p[0] == workload and p[1] == launch and p[2] == digest:
-                return int(p[3]) + int(p[4])
+                return int(p[3]) + (int(p[4]) if kind == "total" else 0)
     return None
 
 
-def run_gpu(args):
-    import torch
-    import torch.distributed as dist
+# ---------------------------------------------------------------------------------------------- GPU
 
-    import moe_prefill_nvfp4_gb300 as moe
-    from moe_prefill_nvfp4_gb300.weights import upload_projection
 
-    ws_n, rank, local = _dist()
-    torch.cuda.set_device(local)
-    if ws_n > 1:
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    case = build_case(args.workload)
-    T, H, I, E, k = case.T, case.H, case.I, case.E, case.k
-    x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
-    wr = torch.from_numpy(case.router_w.view(np.int16)).view(torch.bfloat16).to(dev) if case.router_w is not None else None
-    logits = torch.from_numpy(case.logits).to(dev) if case.logits is not None else None
-    gu = upload_projection(case.gate_up.packed, case.gate_up.scales, case.gate_up.scale2, 2 * I, H, device=str(dev))
-    dn = upload_projection(case.down.packed, case.down.scales, case.down.scale2, H, I, device=str(dev))
-    cfg = moe.MoePrefillConfig(hidden=H, moe_intermediate=I, num_experts=E, top_k=k, swiglu_limit=7.0,
-                               renormalize=1, routed_scale=1.0)
-    lay = moe.moe_workspace_layout(cfg, T)
-    ws = torch.empty(lay.total, dtype=torch.uint8, device=dev)
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    NEV = moe.MOE_FWD_NUM_EVENTS
-    sh = None
-    if case.shared is not None:  # shared expert on a second stream, joined before the combine
-        bits = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-        sh = dict(gate=bits(case.shared.gate), up=bits(case.shared.up), down=bits(case.shared.down),
-                  out=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
-                  ws=torch.empty(moe.moe_shared_expert_workspace_bytes(T, H, case.shared.I), dtype=torch.uint8,
-                                 device=dev),
-                  side=torch.cuda.Stream(dev), fork=torch.cuda.Event(), ready=torch.cuda.Event())
+class GpuBench:
+    """Device state shared by the workloads of one run: the flush buffer, peaks, the stream."""
 
-    def step(events=None, st=None, dst=None, src=None, lg=None):
-        st = st if st is not None else stream
-        dst = dst if dst is not None else out
-        src = src if src is not None else x
-        lg = lg if lg is not None else logits
-        ready = None
-        if sh is not None:
-            sh["fork"].record(st)
-            sh["side"].wait_event(sh["fork"])
-            moe.moe_shared_expert_forward(x, sh["gate"], sh["up"], sh["down"], 7.0, ws=sh["ws"], out=sh["out"],
-                                          stream=sh["side"])
-            sh["ready"].record(sh["side"])
-            ready = sh["ready"]
-        moe.moe_prefill_forward(cfg, src, gu.table, dn.table, ws, w_router=wr, logits=lg, out=dst,
-                                stage_events=events, stream=st, shared_out=sh["out"] if sh else None,
-                                shared_ready=ready)
-        if sh is not None:
-            st.wait_stream(sh["side"])
+    def __init__(self, args, dev):
+        import torch
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    if moe.moe_get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        self.torch = torch
+        self.args = args
+        self.dev = dev
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.peaks, self.peak_src = _peaks()
 
-    # The forward makes no host round trip, so one chunk's whole forward is captured once into a
-    # CUDA graph and replayed per step (the launch-bound host work is paid once, as a serving
-    # loop with fixed chunk shapes does).  A second graph carries the per-stage events.
-    x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    lg_host = torch.from_numpy(case.logits).pin_memory() if case.logits is not None else None
-    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(NEV)]
-    for e in stage_ev:  # torch creates the CUDA event on first record; the library records it afterwards
-        e.record(stream)
-    torch.cuda.synchronize()
-    cap = torch.cuda.Stream(dev)
+    def timed(self, run, n):
+        """n runs, each bracketed by CUDA events on the launching stream, L2 flushed before each
+        (outside the events)."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            self.flush.fill_(1)
+            evs[i][0].record(self.stream)
+            run()
+            evs[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
 
-    def capture(fn):
+    def capture(self, fn):
+        torch = self.torch
+        cap = torch.cuda.Stream(self.dev)
         g = torch.cuda.CUDAGraph()
-        cap.wait_stream(stream)
+        cap.wait_stream(self.stream)
         with torch.cuda.graph(g, stream=cap):
             fn(cap)
         torch.cuda.synchronize()
         return g
 
-    def e2e_body(st):
-        # The step's inputs and result live in pinned host memory, which the device reaches over
-        # the coherent CPU-GPU link: the forward stages x into its workspace as the router reads
-        # it (without a router, with one copy), the top-k reads host logits in place and the
-        # combine stores out into the host buffer.  With a shared expert (which reads x from
-        # device memory) x is copied to the device first.
-        if sh is not None:
-            x.copy_(x_host, non_blocking=True)
-            step(None, st, dst=out_host, lg=lg_host)
-        else:
-            step(None, st, dst=out_host, src=x_host, lg=lg_host)
+    # -------------------------------------------------------------------------- a routed block
 
-    g_step = capture(lambda st: step(None, st))
-    g_stage = capture(lambda st: step(stage_ev, st))
-    g_e2e = capture(e2e_body)
-    for g in (g_step, g_stage, g_e2e):
-        for _ in range(3):
-            flush.fill_(1)
+    def block(self, name: str, case, steps: int, warmup: int, e2e: bool = True, clocks=None, tag=None) -> dict:
+        """Time one routed-MoE block workload: graph replays of the forward (value), the stage
+        graph (per-stage times and the GEMM rooflines), the end-to-end graph on pinned host
+        buffers, and eager launches."""
+        import moe_prefill_nvfp4_gb300 as moe
+        from moe_prefill_nvfp4_gb300.weights import upload_projection
+
+        torch = self.torch
+        dev = self.dev
+        T, H, I, E, k = case.T, case.H, case.I, case.E, case.k
+        x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        wr = (torch.from_numpy(case.router_w.view(np.int16)).view(torch.bfloat16).to(dev)
+              if case.router_w is not None else None)
+        logits = torch.from_numpy(case.logits).to(dev) if case.logits is not None else None
+        gu = getattr(case, "_dev_gu", None) or upload_projection(case.gate_up.packed, case.gate_up.scales,
+                                                                 case.gate_up.scale2, 2 * I, H, device=str(dev))
+        dn = getattr(case, "_dev_dn", None) or upload_projection(case.down.packed, case.down.scales, case.down.scale2,
+                                                                 H, I, device=str(dev))
+        cfg = moe.MoePrefillConfig(hidden=H, moe_intermediate=I, num_experts=E, top_k=k, swiglu_limit=7.0,
+                                   renormalize=1, routed_scale=1.0)
+        lay = moe.moe_workspace_layout(cfg, T)
+        ws = torch.empty(lay.total, dtype=torch.uint8, device=dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        NEV = moe.MOE_FWD_NUM_EVENTS
+        sh = None
+        if case.shared is not None:  # shared expert on a second stream, joined before the combine
+            bits = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            sh = dict(gate=bits(case.shared.gate), up=bits(case.shared.up), down=bits(case.shared.down),
+                      out=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                      ws=torch.empty(moe.moe_shared_expert_workspace_bytes(T, H, case.shared.I), dtype=torch.uint8,
+                                     device=dev),
+                      side=torch.cuda.Stream(dev), fork=torch.cuda.Event(), ready=torch.cuda.Event())
+
+        def step(events=None, st=None, dst=None, src=None, lg=None):
+            st = st if st is not None else self.stream
+            dst = dst if dst is not None else out
+            src = src if src is not None else x
+            lg = lg if lg is not None else logits
+            ready = None
+            if sh is not None:
+                sh["fork"].record(st)
+                sh["side"].wait_event(sh["fork"])
+                moe.moe_shared_expert_forward(x, sh["gate"], sh["up"], sh["down"], 7.0, ws=sh["ws"], out=sh["out"],
+                                              stream=sh["side"])
+                sh["ready"].record(sh["side"])
+                ready = sh["ready"]
+            moe.moe_prefill_forward(cfg, src, gu.table, dn.table, ws, w_router=wr, logits=lg, out=dst,
+                                    stage_events=events, stream=st, shared_out=sh["out"] if sh else None,
+                                    shared_ready=ready)
+            if sh is not None:
+                st.wait_stream(sh["side"])
+
+        for _ in range(warmup):
+            self.flush.fill_(1)
+            step()
+        torch.cuda.synchronize()
+        if moe.moe_get_device_error() != 0:
+            raise RuntimeError(f"{name}: device error during warm-up")
+
+        # The forward makes no host round trip, so one chunk's whole forward is captured once into
+        # a CUDA graph and replayed per step (the launch-bound host work is paid once, as a serving
+        # loop with fixed chunk shapes does).  A second graph carries the per-stage events.
+        stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(NEV)]
+        for e in stage_ev:  # torch creates the CUDA event on first record; the library records it afterwards
+            e.record(self.stream)
+        torch.cuda.synchronize()
+        g_step = self.capture(lambda st: step(None, st))
+        g_stage = self.capture(lambda st: step(stage_ev, st))
+        graphs = [g_step, g_stage]
+        if e2e:
+            x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+            lg_host = torch.from_numpy(case.logits).pin_memory() if case.logits is not None else None
+            out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+
+            def e2e_body(st):
+                # The step's inputs and result live in pinned host memory, which the device reaches
+                # over the coherent CPU-GPU link: the forward stages x into its workspace as the router
+                # reads it (without a router, with one copy), the top-k reads host logits in place and
+                # the combine stores out into the host buffer.  With a shared expert (which reads x
+                # from device memory) x is copied to the device first.
+                if sh is not None:
+                    x.copy_(x_host, non_blocking=True)
+                    step(None, st, dst=out_host, lg=lg_host)
+                else:
+                    step(None, st, dst=out_host, src=x_host, lg=lg_host)
+
+            g_e2e = self.capture(e2e_body)
+            graphs.append(g_e2e)
+        for g in graphs:
+            for _ in range(3):
+                self.flush.fill_(1)
+                g.replay()
+        torch.cuda.synchronize()
+
+        if clocks is not None:
+            clocks.start()
+            time.sleep(0.3)
+        t_wall0 = time.perf_counter()
+        step_ms = self.timed(g_step.replay, steps)
+        t_wall = time.perf_counter() - t_wall0
+        # per-stage times: the same graph with the stage events, one step at a time
+        stage_rows = []
+        for _ in range(steps):
+            self.flush.fill_(1)
+            g_stage.replay()
+            torch.cuda.synchronize()
+            stage_rows.append([stage_ev[j].elapsed_time(stage_ev[j + 1]) for j in range(NEV - 1)])
+        stage_ms = np.array(stage_rows)
+        e2e_list = self.timed(g_e2e.replay, steps) if e2e else None
+        eager_list = self.timed(step, steps)
+        clk = clocks.stop() if clocks is not None else None
+        if moe.moe_get_device_error() != 0:
+            raise RuntimeError(f"{name}: device error during timed steps")
+        total_ms = max_over_ranks(float(sum(step_ms)), dev)
+        eager_ms = max_over_ranks(float(sum(eager_list)), dev)
+
+        off = ws[lay.expert_offsets:lay.expert_offsets + 4 * (E + 1)].view(torch.int32).cpu().numpy()
+        # stage intervals between the forward's 8 events; with a router (E <= 64) the router GEMM and
+        # the top-k are one launch ("route_topk" is then an empty interval), and with the fused SwiGLU
+        # the "swiglu" interval is empty (each interval carries the event node's own ~2 us)
+        names = ["router_logits", "route_topk", "sort", "grouped_gemm_gate_up", "swiglu", "grouped_gemm_down",
+                 "combine"]
+        mean_stage = stage_ms.mean(axis=0)
+        gemms = {}
+        for proj, idx in (("gate_up", 3), ("down", 5)):
+            gemms[proj] = roofline_entry(f"grouped_gemm_{proj}", gemm_bytes(case, off, proj), gemm_flops(case, proj),
+                                         mean_stage[idx] / 1e3, self.peaks, self.peak_src,
+                                         measured_traffic(tag or name, proj))
+        dom = "gate_up" if mean_stage[3] >= mean_stage[5] else "down"
+        R = T * k
+        launches = (((2 if E > 64 else 1) if wr is not None else 1) + (1 if R <= 2048 else 2) + 3
+                    + (1 if sh is not None else 0))
+        res = {
+            "workload": WORKLOAD_DESC.get(name, name), "rows": T, "hidden": H, "moe_intermediate": I, "experts": E,
+            "top_k": k, "experts_touched": int((np.diff(off[:E + 1]) > 0).sum()),
+            "max_rows_per_expert": int(np.diff(off[:E + 1]).max()),
+            "value": round(replica_throughput(1, T, steps, total_ms), 1), "unit": "tokens/s",
+            "ms_per_step": round(total_ms / steps, 5),
+            "routed_tflops": round((gemm_flops(case, "gate_up") + gemm_flops(case, "down")) / (total_ms / steps / 1e3)
+                                   / 1e12, 1),
+            "eager": {"value": round(replica_throughput(1, T, steps, eager_ms), 1), "unit": "tokens/s",
+                      "ms_per_step": round(eager_ms / steps, 5),
+                      "how": "moe_prefill_forward launched from the host every step (no graph)"},
+            "roofline": gemms[dom],
+            "gemm_roofline": gemms,
+            "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
+            # routing (router GEMM + top-k as one launch for E <= 64, else two; top-k alone on given
+            # logits), sort (one launch up to 2048 slots, else two), gate/up GEMM with the fused
+            # SwiGLU, down GEMM, combine (+ the shared expert's SwiGLU; its GEMMs are cuBLAS kernels)
+            "gpu_launches_per_step": launches,
+            "wall_s_timed": round(t_wall, 4),
+        }
+        if e2e:
+            e2e_ms = max_over_ranks(float(sum(e2e_list)), dev)
+            res["e2e"] = {"value": round(replica_throughput(1, T, steps, e2e_ms), 1), "unit": "tokens/s",
+                          "h2d_bytes_per_step": x_host.numel() * 2 + (lg_host.numel() * 4 if lg_host is not None else 0),
+                          "d2h_bytes_per_step": out_host.numel() * 2,
+                          "how": "CUDA graph of moe_prefill_forward on pinned host x/logits/out (x staged to the "
+                                 "device by the router kernel or one copy, logits read in place, out stored by the "
+                                 "combine), replayed per step"}
+        if clk is not None:
+            res["clocks"] = clk
+        del ws, out
+        if getattr(case, "_dev_gu", None) is None:
+            gu.close()
+            dn.close()
+        return res
+
+    # --------------------------------------------------------------------- the single GEMM (c0)
+
+    def single_gemm(self, steps: int) -> dict:
+        """c0: one grouped W4A16 GEMM launch over 512 gathered rows.  Its algorithmic time is far
+        below a launch (0.15 us of HBM at the measured peak), so the number is launch latency:
+        a graph of one launch replayed per step (L2 flushed), and a graph of 20 back-to-back
+        launches (L2 warm after the first) for the per-launch cost in a stream."""
+        import moe_prefill_nvfp4_gb300 as moe
+        from moe_prefill_nvfp4_gb300.weights import upload_projection
+        from synth import inputs as S
+
+        torch = self.torch
+        c = S.workload("c0")
+        dev = self.dev
+        A = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        ids = torch.from_numpy(c.ids).to(dev)
+        w = upload_projection(c.w.packed, c.w.scales, c.w.scale2, c.N, c.K, device=str(dev))
+        srt = moe.moe_sort_by_expert(ids, c.E)
+        R = c.T * c.k
+        C = torch.empty(R, c.N, dtype=torch.bfloat16, device=dev)
+
+        def one(st):
+            moe.moe_w4a16_grouped_gemm(A, w.table, srt["expert_offsets"], R, gather_ids=srt["sorted_token_ids"],
+                                       out=C, stream=st)
+
+        for _ in range(5):
+            one(self.stream)
+        torch.cuda.synchronize()
+        g1 = self.capture(one)
+        nb = 20
+        g20 = self.capture(lambda st: [one(st) for _ in range(nb)])
+        for g in (g1, g20):
             g.replay()
-    torch.cuda.synchronize()
-
-    def timed(run, n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        for i in range(n):
-            flush.fill_(1)  # L2 flush, outside the step's events
-            evs[i][0].record(stream)
-            run()
-            evs[i][1].record(stream)
         torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
+        cold = self.timed(g1.replay, steps)
+        burst = self.timed(g20.replay, max(3, steps // 4))
+        if moe.moe_get_device_error() != 0:
+            raise RuntimeError("c0: device error")
+        off = srt["expert_offsets"].cpu().numpy()
+        touched = int((np.diff(off) > 0).sum())
+        nbytes = weight_bytes_min(touched, c.N, c.K) + c.T * c.K * 2 + R * c.N * 2
+        flops = 2 * R * c.N * c.K
+        us_cold = float(np.mean(cold)) * 1e3
+        us_burst = float(np.mean(burst)) * 1e3 / nb
+        w.close()
+        return {"workload": C0_DESC, "rows": c.T, "sorted_rows": R, "experts": c.E, "top_k": c.k, "N": c.N, "K": c.K,
+                "bound": "latency", "us_per_launch_cold": round(us_cold, 2),
+                "us_per_launch_back_to_back": round(us_burst, 2),
+                "tflops_back_to_back": round(flops / (us_burst * 1e-6) / 1e12, 3),
+                "gbs_back_to_back": round(nbytes / (us_burst * 1e-6) / 1e9, 1),
+                "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                "roofline_us": round(max(nbytes / (self.peaks["hbm_gbs"] * 1e9),
+                                         flops / (self.peaks["bf16_tflops"] * 1e12)) * 1e6, 3),
+                "note": "the roofline time is far below one launch: the launch latency binds, 70% of roofline "
+                        "is unreachable at this size",
+                "how": "CUDA events around a graph of one launch (L2 flushed before each) and around a graph of "
+                       f"{nb} back-to-back launches"}
 
+    # --------------------------------------------------------------------------- the sweep (c4)
+
+    def sweep(self, rows, steps: int, warmup: int) -> list:
+        """c4: the forward at each row count, one set of GLM-shape expert weights (seed of the
+        sweep) on the device for every point."""
+        from moe_prefill_nvfp4_gb300.weights import upload_projection
+        from synth import inputs as S
+
+        base = S.workload("c4", T=8)
+        H, I = base.H, base.I
+        gu = upload_projection(base.gate_up.packed, base.gate_up.scales, base.gate_up.scale2, 2 * I, H,
+                               device=str(self.dev))
+        dn = upload_projection(base.down.packed, base.down.scales, base.down.scale2, H, I, device=str(self.dev))
+        out = []
+        for T in rows:
+            c = S.make_block_case(T=T, H=H, I=I, E=base.E, k=base.k, routing="biased", seed=S.WORKLOADS["c4"]["seed"],
+                                  with_weights=False)
+            c.gate_up, c.down = base.gate_up, base.down
+            c._dev_gu, c._dev_dn = gu, dn
+            r = self.block(f"c4 T={T}", c, steps, warmup, e2e=False, tag=f"c4_{T}")
+            entry = {"rows": T, "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+                     "routed_tflops": r["routed_tflops"], "experts_touched": r["experts_touched"],
+                     "stage_ms": {k2: r["stage_ms"][k2] for k2 in ("grouped_gemm_gate_up", "grouped_gemm_down")}}
+            for proj in ("gate_up", "down"):
+                g = r["gemm_roofline"][proj]
+                N, K = (2 * I, H) if proj == "gate_up" else (H, I)
+                bmin = weight_bytes_min(r["experts_touched"], N, K)
+                read = measured_traffic(f"c4_{T}", proj, kind="read")
+                entry[proj] = {"bound": g["bound"], "frac": g["frac"], "achieved": g["achieved"], "unit": g["unit"],
+                               "us": g["us"], "weight_bytes_min": bmin,
+                               "weight_bytes_read": read if read is not None else bmin,
+                               "weight_bytes_read_source": ("ncu dram__bytes_read.sum (all bytes of the launch)"
+                                                            if read is not None else
+                                                            "algorithmic: each touched expert once (no capture of "
+                                                            "the current kernel at this row count)")}
+            out.append(entry)
+        gu.close()
+        dn.close()
+        return out
+
+
+def run_gpu(args):
+    import torch
+
+    import moe_prefill_nvfp4_gb300 as moe  # noqa: F401  (loads the library)
+    from synth import inputs as S
+
+    ws_n, rank, local = _dist()
+    if ws_n > 1 or args.gpus > 1:
+        print("bench.py runs on one GPU: the grouped GEMM multicasts activation rows within a thread-block "
+              "cluster, which stays in single-GPU runs", file=sys.stderr)
+        sys.exit(2)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gb = GpuBench(args, dev)
     clocks = ClockSampler(local)
-    if ws_n > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    t_wall0 = time.perf_counter()
-    step_ms = timed(g_step.replay, args.steps)
-    t_wall = time.perf_counter() - t_wall0
-    # per-stage times: the same graph with the stage events, one step at a time
-    stage_rows = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        g_stage.replay()
-        torch.cuda.synchronize()
-        stage_rows.append([stage_ev[j].elapsed_time(stage_ev[j + 1]) for j in range(NEV - 1)])
-    stage_ms = np.array(stage_rows)
-    # end to end: pinned host x (and logits) -> device, forward, out -> pinned host, every step
-    e2e_list = timed(g_e2e.replay, args.steps)
-    # the same forward launched eagerly from the host every step (no graph)
-    eager_list = timed(step, args.steps)
-    clk = clocks.stop()
-    if moe.moe_get_device_error() != 0:
-        raise RuntimeError("device error during timed steps")
-    total_ms = max_over_ranks(float(sum(step_ms)), dev)
-    value = replica_throughput(ws_n, T, args.steps, total_ms)
-    e2e_ms = max_over_ranks(float(sum(e2e_list)), dev)
-    eager_ms = max_over_ranks(float(sum(eager_list)), dev)
-    h2d = x_host.numel() * 2 + (lg_host.numel() * 4 if lg_host is not None else 0)
-    d2h = out_host.numel() * 2
-
-    # ---- roofline of the dominant kernel (largest mean stage time)
-    off = ws[lay.expert_offsets:lay.expert_offsets + 4 * (E + 1)].view(torch.int32).cpu().numpy()
-    # stage intervals between the forward's 8 events; with a router (E <= 64) the router GEMM and the top-k
-    # are one launch ("route_topk" is then an empty interval), and with the fused SwiGLU the
-    # "swiglu" interval is empty (each interval carries the event node's own ~2 us)
-    names = ["router_logits", "route_topk", "sort", "grouped_gemm_gate_up", "swiglu", "grouped_gemm_down", "combine"]
-    mean_stage = stage_ms.mean(axis=0)
-    dom = int(np.argmax(mean_stage))
-    peaks, src = _peaks()
-    R = T * k
-    flops = {"grouped_gemm_gate_up": 2 * R * 2 * I * H, "grouped_gemm_down": 2 * R * H * I}
-    bytes_ = {"grouped_gemm_gate_up": gemm_bytes(case, off, "gate_up"), "grouped_gemm_down": gemm_bytes(case, off, "down")}
-    dname = names[dom]
-    dur_s = mean_stage[dom] / 1e3
-    roof = None
-    traffic = measured_traffic(args.workload, dname.replace("grouped_gemm_", "")) if dname in bytes_ else None
-    if dname in bytes_:
-        t_hbm = bytes_[dname] / (peaks["hbm_gbs"] * 1e9)
-        t_tc = flops[dname] / (peaks["bf16_tflops"] * 1e12)
-        if t_hbm >= t_tc:
-            ach = bytes_[dname] / dur_s / 1e9
-            roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
-                    "algorithmic_bytes": bytes_[dname], "peak_source": src}
-        else:
-            ach = flops[dname] / dur_s / 1e12
-            roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
-                    "algorithmic_flops": flops[dname], "peak_source": src}
+    head = gb.block(args.workload, S.workload(args.workload), args.steps, args.warmup, clocks=clocks)
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(S.workload(args.workload), args.cpu_budget_s)
+    reports = [r for r in args.reports.split(",") if r and r != "none"]
+    extra = {}
+    c0 = None
+    sweep = None
+    for r in reports:
+        if r in ("c1", "c2", "c1s"):
+            case = S.workload(r)
+            extra[r] = gb.block(r, case, args.steps, args.warmup)
+            if not args.no_cpu_baseline:
+                extra[r]["cpu_baseline"] = cpu_baseline(case, args.cpu_budget_s)
+        elif r == "c0":
+            c0 = gb.single_gemm(args.steps)
+        elif r == "c4":
+            rows = S.SWEEP_ROWS if args.sweep_rows is None else tuple(int(v) for v in args.sweep_rows.split(","))
+            sweep = gb.sweep(rows, max(3, args.steps // 2), 3)
     res = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (NVFP4 weights dequantised to BF16, FP32 accumulate)",
         "data": "synthetic (seeded; random NVFP4 weights, no trained checkpoint)",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "rows": T, "hidden": H, "moe_intermediate": I,
-                   "experts": E, "top_k": k, "parallelism": f"replicas x{ws_n}",
+        "config": {"workload": head["workload"], "rows": head["rows"], "hidden": head["hidden"],
+                   "moe_intermediate": head["moe_intermediate"], "experts": head["experts"], "top_k": head["top_k"],
                    "l2": "flushed between timed steps (256 MiB write outside the step events)"},
-        "e2e": {"value": round(replica_throughput(ws_n, T, args.steps, e2e_ms), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "CUDA graph of moe_prefill_forward on pinned host x/logits/out (x staged to the device "
-                       "by the router kernel or one copy, logits read in place, out stored by the combine), "
-                       "replayed per step"},
-        "eager": {"value": round(replica_throughput(ws_n, T, args.steps, eager_ms), 1), "unit": "tokens/s",
-                  "ms_per_step": round(eager_ms / args.steps, 5),
-                  "how": "moe_prefill_forward launched from the host every step (no graph)"},
+        "e2e": head["e2e"],
+        "eager": head["eager"],
         "timing": "CUDA events around each graph replay of the forward; stage_ms from a second graph with "
                   "stage events, replayed one step at a time",
-        "roofline": roof,
-        "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
-        # routing (router GEMM + top-k as one launch for E <= 64, else two; top-k alone on given
-        # logits), sort (one launch up to 2048 slots, else two), gate/up GEMM with the fused
-        # SwiGLU, down GEMM, combine (+ the shared expert's SwiGLU; its GEMMs are cuBLAS kernels)
-        "gpu_launches": (((2 if E > 64 else 1) if wr is not None else 1) + (1 if T * k <= 2048 else 2) + 3
-                         + (1 if sh is not None else 0)) * args.steps,
-        "clocks": clk,
-        "wall_s_timed": round(t_wall, 4),
+        "roofline": head["roofline"],
+        "gemm_roofline": head["gemm_roofline"],
+        "stage_ms": head["stage_ms"],
+        "routed_tflops": head["routed_tflops"],
+        "experts_touched": head["experts_touched"],
+        "max_rows_per_expert": head["max_rows_per_expert"],
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "clocks": head.get("clocks"),
+        "wall_s_timed": head["wall_s_timed"],
     }
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(case, args.cpu_budget_s)
-    gu.close()
-    dn.close()
-    if ws_n > 1:
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(res), flush=True)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if extra:
+        res["workloads"] = extra
+    if c0 is not None:
+        res["c0"] = c0
+    if sweep is not None:
+        res["c4_sweep"] = {"workload": C4_DESC, "points": sweep}
+    print(json.dumps(res), flush=True)
 
 
 # ---------------------------------------------------------------------------------------------- CPU
@@ -414,50 +612,78 @@ def _blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_sample_rows(case) -> int:
+    """Rows of one bounded oracle sample: the whole chunk for the 256-row block, one row at GLM
+    shapes (where the oracle's per-expert dequantisation of the 8 touched experts alone takes
+    seconds)."""
+    return case.T if case.H * case.I <= 2048 * 768 else 1
+
+
+def _head_rows(case, n: int):
+    """The first n rows of a block workload (same weights)."""
+    import copy
+
+    c = copy.copy(case)
+    c.T = n
+    c.x = case.x[:n]
+    if case.logits is not None:
+        c.logits = case.logits[:n]
+    return c
+
+
 def cpu_baseline(case, budget_s: float = 20.0) -> dict:
-    """The oracle (BF16 variant) as it stands, on the host cores: whole chunks while the budget
-    lasts (at least one).  Returns tokens/s of the oracle."""
+    """The oracle (BF16 variant) as it stands, on the host cores: samples of the workload's first
+    rows while the budget lasts (at least one).  Returns tokens/s of the oracle."""
     from oracle import moe_oracle as O
 
+    n_rows = oracle_sample_rows(case)
+    sub = _head_rows(case, n_rows)
     t0 = time.perf_counter()
     n = 0
     while True:
-        O.prefill_forward(case, "bf16")
+        O.prefill_forward(sub, "bf16")
         n += 1
         if time.perf_counter() - t0 > budget_s / 2 or n >= 3:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(n * case.T / dt, 2), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{n} full {case.T}-row chunk(s) of the same workload through the fp64 numpy oracle "
-                      f"(BF16 variant), {dt:.1f} s; numpy elementwise single-threaded, BLAS matmuls on the cores listed"}
+    what = f"{n} full {case.T}-row chunk(s)" if n_rows == case.T else \
+        f"{n} sample(s) of the chunk's first {n_rows} row(s) (each its own oracle call, dequantising its experts)"
+    return {"value": round(n * n_rows / dt, 3), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{what} of the same workload through the fp64 numpy oracle (BF16 variant), {dt:.1f} s; "
+                      f"numpy elementwise single-threaded, BLAS matmuls on the cores listed"}
 
 
 def run_reference(args):
     ws_n, rank, _ = _dist()
     if rank != 0:
         return
-    case = build_case(args.workload)
+    from synth import inputs as S
+
+    case = S.workload(args.workload)
     from oracle import moe_oracle as O
 
-    # The oracle holds no warm state: one untimed chunk warms imports and page faults; the
+    n_rows = oracle_sample_rows(case)
+    sub = _head_rows(case, n_rows)
+    # The oracle holds no warm state: one untimed sample warms imports and page faults; the
     # remaining warm-up steps would only repeat it.
     if args.warmup > 0:
-        O.prefill_forward(case, "bf16")
+        O.prefill_forward(sub, "bf16")
     t0 = time.perf_counter()
-
     for _ in range(args.steps):
-        O.prefill_forward(case, "bf16")
+        O.prefill_forward(sub, "bf16")
     dt = time.perf_counter() - t0
-    value = case.T * args.steps / dt
-    res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws_n,
+    value = n_rows * args.steps / dt
+    what = f"{args.steps} full {case.T}-row chunk(s), one per step" if n_rows == case.T else \
+        f"{args.steps} samples of the chunk's first {n_rows} row(s), one per step"
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws_n,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded)",
            "config": {"workload": WORKLOAD_DESC[args.workload], "rows": case.T, "hidden": case.H,
                       "moe_intermediate": case.I, "experts": case.E, "top_k": case.k},
-           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-                            "sample": f"{args.steps} full {case.T}-row chunk(s), one per step"},
-           "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                            "sample": what},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
@@ -467,7 +693,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c1", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--reports", default="c1,c2,c0,c4",
+                    help="extra workloads in the same line: any of c0,c1,c2,c1s,c4 (comma-separated) or none")
+    ap.add_argument("--sweep-rows", default=None, help="row counts of the c4 sweep (default: all eleven)")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

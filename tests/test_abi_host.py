@@ -60,7 +60,9 @@ def test_sort_noalloc_rejects_before_any_launch(L):
     assert _lib.MOE_SORT_NOALLOC_MAX_INTS == 65536
     assert L.moe_sort_by_expert_noalloc(P, 104200, 8, 160, P, P, P, P, NULL) == 7
     assert L.moe_sort_by_expert_noalloc(P, 833537, 1, 160, P, P, P, P, NULL) == 7
-    assert L.moe_sort_by_expert_noalloc(P, 2048, 8, 1024, P, P, P, P, NULL) != 7  # 1025 * 8 fits
+    # 1025 * 8 counts fit: checked on the host sizes alone (a call would launch on a GPU machine)
+    assert L.moe_sort_workspace_bytes(2048, 8, 1024) <= 4 * _lib.MOE_SORT_NOALLOC_MAX_INTS
+    assert L.moe_sort_workspace_bytes(104200, 8, 160) > 4 * _lib.MOE_SORT_NOALLOC_MAX_INTS
 
 
 def test_gemm_and_elementwise_reject(L):

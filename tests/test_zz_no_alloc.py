@@ -1,8 +1,9 @@
 """moe_sort_by_expert_noalloc: the expert sort on the library's fixed device scratch.
 
-Compared bit-exactly with moe_sort_by_expert (caller workspace) on two calls issued back to
-back on one stream, which reuse the same scratch; the file is named to be collected last so it
-also runs after every other GPU test in the session.
+Compared bit-exactly with moe_sort_by_expert (caller workspace) and with the oracle's stable
+counting sort on two calls issued back to back on one stream, which reuse the same scratch;
+the file is named to be collected last so it also runs after every other GPU test in the
+session.
 """
 
 import numpy as np
@@ -12,6 +13,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 import moe_prefill_nvfp4_gb300 as moe  # noqa: E402
+from oracle import moe_oracle as O  # noqa: E402
 from synth import inputs as S  # noqa: E402
 
 KEYS = ("sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm")
@@ -25,8 +27,6 @@ def _no_device_error():
 
 
 def _ids_glm(T=2048, E=160, k=8):
-    from oracle import moe_oracle as O
-
     case = S.workload("c2")
     ids, _ = O.route_topk(case.logits[:T], k)
     return torch.from_numpy(ids).cuda(), E
@@ -62,6 +62,10 @@ def test_two_calls_in_a_row_match_the_workspace_sort():
         torch.cuda.synchronize()
         for key in KEYS:
             assert torch.equal(out[key], ref[key]), key
+        # and directly against the oracle's stable counting sort, bit for bit
+        srt = O.sort_by_expert(ids.cpu().numpy(), E)
+        for key in KEYS:
+            np.testing.assert_array_equal(out[key].cpu().numpy().reshape(srt[key].shape), srt[key], err_msg=key)
 
 
 def test_repeated_call_is_identical():

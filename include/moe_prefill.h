@@ -363,12 +363,49 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
  * `ready`: INT32 [E + 1], per-expert counters through which the down GEMM starts on an expert as
  * soon as the gate/up GEMM has stored its activation rows, and the down GEMM's dynamic tile
  * counter (cleared by the sort on every call).  `x_stage`: BF16 [T, H], the device copy of an x
- * passed in host memory (unused when x is device memory). */
+ * passed in host memory (unused when x is device memory).  `x_sorted`: BF16 [T * top_k, H], the
+ * token rows in expert order (row p = x[sorted_token_ids[p]]) that the CTA-pair gate/up GEMM
+ * reads (unused with the single-CTA kernel, which gathers inside the GEMM). */
 typedef struct {
   size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, ready,
-      G, act, Y, x_stage, total;
+      G, act, Y, x_stage, x_sorted, total;
 } moe_workspace_layout_t;
 int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_workspace_layout_t* layout);
+
+/* ---------------------------------------------------------------- debug controls */
+/*
+ * Test and debug settings of the whole process (no counterpart on the pages).  They change
+ * which code runs or how long it waits, never what it computes; both are process-global and
+ * take effect for the launches issued after the call.
+ *
+ * moe_debug_set_gemm_kernel: which grouped GEMM kernel the GEMM entry points and the forward
+ * launch.  MOE_GEMM_KERNEL_AUTO (the default) takes the CTA-pair kernel wherever its shapes
+ * allow (N % 256 == 0; with the fused SwiGLU I % 128 == 0) and the single-CTA kernel otherwise;
+ * SINGLE always takes the single-CTA kernel; PAIR makes the entry points return
+ * MOE_ERR_UNSUPPORTED_SHAPE for shapes the pair kernel does not take.  Returns
+ * MOE_ERR_INVALID_ARG for another value.
+ *
+ * moe_debug_set_wait_limit_ns: the bound of every pipeline wait of the CTA-pair kernel
+ * (default and maximum 2 s; 0 restores the default).  After the bound a waiting kernel records
+ * MOE_DEVERR_TIMEOUT, drains its copies and MMAs and returns.  Returns the previous bound.
+ */
+#define MOE_GEMM_KERNEL_AUTO 0
+#define MOE_GEMM_KERNEL_SINGLE 1
+#define MOE_GEMM_KERNEL_PAIR 2
+int moe_debug_set_gemm_kernel(int which);
+unsigned long long moe_debug_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * moe_debug_grouped_gemm_after: moe_w4a16_grouped_gemm as the consumer side of the forward's GEMM
+ * overlap: expert e's A rows are read only once ready[e] >= rows_e * ready_need * 4 (the count a
+ * producer GEMM's epilogue warps publish as they store those rows; ready device int32 [E]).  For
+ * the failure-path tests: counters that never reach the count make the wait run out, and the
+ * kernel returns with MOE_DEVERR_TIMEOUT after the wait bound.  Other arguments as
+ * moe_w4a16_grouped_gemm; MOE_ERR_INVALID_ARG for a NULL ready or ready_need < 1.
+ */
+int moe_debug_grouped_gemm_after(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                 const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
+                                 int c_dtype, const int32_t* ready, int ready_need, void* stream);
 
 /* ---------------------------------------------------------------- errors */
 /*

@@ -27,6 +27,8 @@ __all__ = [
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
     "moe_shared_expert_workspace_bytes", "moe_shared_expert_forward",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
+    "moe_debug_set_gemm_kernel", "moe_debug_set_wait_limit_ns", "MOE_GEMM_KERNEL_AUTO", "MOE_GEMM_KERNEL_SINGLE",
+    "MOE_GEMM_KERNEL_PAIR", "gemm_kernel", "moe_debug_grouped_gemm_after",
 ]
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_prefill.h")
@@ -38,6 +40,9 @@ MOE_FWD_NUM_EVENTS = 8
 MOE_FWD_SEPARATE_SWIGLU = 1  # moe_prefill_config.flags: SwiGLU as its own kernel on a materialised G
 MOE_FWD_SMALL_ROWS = 2  # moe_prefill_config.flags: small-row products (FP32 weights) for chunks of <= 8 rows
 MOE_SORT_NOALLOC_MAX_INTS = 65536  # int32 entries of the library's fixed sort scratch
+MOE_GEMM_KERNEL_AUTO = 0  # moe_debug_set_gemm_kernel: CTA-pair kernel where its shapes allow
+MOE_GEMM_KERNEL_SINGLE = 1  # the single-CTA kernel
+MOE_GEMM_KERNEL_PAIR = 2  # the CTA-pair kernel only (other shapes are refused)
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_NOT_BUILT_FOR_DEVICE", 7: "MOE_ERR_SCRATCH_LIMIT"}
 DEVERR = {0: "none", 1: "bad expert id", 2: "bad expert offsets", 3: "pipeline wait timeout", 4: "NaN logit",
@@ -59,7 +64,7 @@ class MoePrefillConfig(ctypes.Structure):
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "ids", "wts", "sorted_token_ids", "sorted_expert_ids",
                                                "expert_offsets", "token_to_perm", "sort_scratch", "ready", "G", "act", "Y",
-                                               "x_stage", "total")]
+                                               "x_stage", "x_sorted", "total")]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -96,6 +101,9 @@ _SIGS = {
     "moe_shared_expert_workspace_bytes": (_SZ, [_I, _I, _I]),
     "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _P, _F, _P, _SZ, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I)]),
+    "moe_debug_set_gemm_kernel": (_I, [_I]),
+    "moe_debug_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
+    "moe_debug_grouped_gemm_after": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _I, _I, _P, _I, _P]),
 }
 
 
@@ -428,3 +436,45 @@ def moe_get_device_error(stream=None) -> int:
     if rc not in (MOE_OK, 5):
         raise MoeError(rc, "moe_get_device_error")
     return int(code.value)
+
+
+def moe_debug_set_gemm_kernel(which: int) -> None:
+    """Process-wide choice of the grouped GEMM kernel (MOE_GEMM_KERNEL_*), for tests and debugging."""
+    _check(lib().moe_debug_set_gemm_kernel(int(which)), "moe_debug_set_gemm_kernel")
+
+
+def moe_debug_set_wait_limit_ns(ns: int) -> int:
+    """Bound of the CTA-pair GEMM's pipeline waits (0 restores 2 s); returns the previous bound."""
+    return int(lib().moe_debug_set_wait_limit_ns(int(ns)))
+
+
+def moe_debug_grouped_gemm_after(A: torch.Tensor, W: ExpertTable, expert_offsets: torch.Tensor, R: int,
+                                 ready: torch.Tensor, ready_need: int, gather_ids: Optional[torch.Tensor] = None,
+                                 out: Optional[torch.Tensor] = None, c_dtype: torch.dtype = torch.float32,
+                                 stream=None) -> torch.Tensor:
+    """The grouped GEMM waiting per expert on producer counters ``ready`` (int32 [E])."""
+    _need(A, torch.bfloat16, "A")
+    _need(ready, torch.int32, "ready")
+    code = MOE_DTYPE_F32 if c_dtype == torch.float32 else MOE_DTYPE_BF16
+    if out is None:
+        out = torch.empty(R, W.N, dtype=c_dtype, device=A.device)
+    _check(lib().moe_debug_grouped_gemm_after(_ptr(A), A.shape[0], A.stride(0), _ptr(gather_ids), W.handle,
+                                              _ptr(expert_offsets), R, _ptr(out), out.stride(0), code, _ptr(ready),
+                                              int(ready_need), _stream(stream)),
+           "moe_debug_grouped_gemm_after")
+    return out
+
+
+class gemm_kernel:
+    """``with gemm_kernel(MOE_GEMM_KERNEL_PAIR): ...`` runs the block with that kernel choice."""
+
+    def __init__(self, which: int):
+        self.which = which
+
+    def __enter__(self):
+        moe_debug_set_gemm_kernel(self.which)
+        return self
+
+    def __exit__(self, *exc):
+        moe_debug_set_gemm_kernel(MOE_GEMM_KERNEL_AUTO)
+        return False

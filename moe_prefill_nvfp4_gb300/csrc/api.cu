@@ -17,7 +17,8 @@
 struct moe_expert_table {
   int E, N, K;
   int device;
-  CUtensorMap* d_maps;    // [E][2]
+  CUtensorMap* d_maps;    // [E][2] (128-row boxes)
+  CUtensorMap* d_maps64;  // [E][2] (64-row boxes, the CTA-pair kernel)
   const void** d_packed;  // [E]
   const void** d_scales;  // [E]
   float* d_scale2;        // [E]
@@ -135,6 +136,16 @@ int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* bas
 
 }  // namespace moe
 
+// Which grouped GEMM kernel runs: the CTA-pair kernel wherever its shapes allow (the default), or
+// the single-CTA kernel (a debug/test setting, moe_debug_set_gemm_kernel).
+namespace moe {
+namespace {
+std::atomic<int> g_gemm_kernel{MOE_GEMM_KERNEL_AUTO};
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+}  // namespace
+uint64_t gemm_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+}  // namespace moe
+
 using namespace moe;
 
 // ==================================================================================================
@@ -176,26 +187,33 @@ int moe_expert_table_create(const void* const* packed, const void* const* scales
   int rc = ensure_device();
   if (rc != MOE_OK) return rc;
 
-  std::vector<CUtensorMap> maps(2 * (size_t)E);
+  // two tensor maps per expert and box height: 128-row boxes (single-CTA kernel), 64-row boxes
+  // (CTA-pair kernel)
+  std::vector<CUtensorMap> maps(2 * (size_t)E), maps64(2 * (size_t)E);
   std::memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
+  std::memset(maps64.data(), 0, maps64.size() * sizeof(CUtensorMap));
   for (int e = 0; e < E; ++e) {
     if (packed[e] == nullptr) continue;
     const cuuint32_t estr[2] = {1, 1};
-    {  // packed nibbles [N, K/2] bytes: box 128 B x 128 rows, 128-byte swizzle
-      const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
-      const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-      const cuuint32_t box[2] = {128, 128};
-      rc = encode_tmap(&maps[2 * e], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(packed[e]), dims, strides,
-                       box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc != MOE_OK) return rc;
-    }
-    {  // E4M3 scales [N, K/16] bytes: box 16 B x 128 rows
-      const cuuint64_t dims[2] = {(cuuint64_t)K / 16, (cuuint64_t)N};
-      const cuuint64_t strides[1] = {(cuuint64_t)K / 16};
-      const cuuint32_t box[2] = {16, 128};
-      rc = encode_tmap(&maps[2 * e + 1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales[e]), dims, strides,
-                       box, estr, CU_TENSOR_MAP_SWIZZLE_NONE);
-      if (rc != MOE_OK) return rc;
+    for (int v = 0; v < 2; ++v) {
+      const cuuint32_t rows = v == 0 ? 128u : 64u;
+      std::vector<CUtensorMap>& dst = v == 0 ? maps : maps64;
+      {  // packed nibbles [N, K/2] bytes: box 128 B x rows, 128-byte swizzle
+        const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+        const cuuint32_t box[2] = {128, rows};
+        rc = encode_tmap(&dst[2 * e], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(packed[e]), dims, strides,
+                         box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != MOE_OK) return rc;
+      }
+      {  // E4M3 scales [N, K/16] bytes: box 16 B x rows
+        const cuuint64_t dims[2] = {(cuuint64_t)K / 16, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K / 16};
+        const cuuint32_t box[2] = {16, rows};
+        rc = encode_tmap(&dst[2 * e + 1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales[e]), dims,
+                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != MOE_OK) return rc;
+      }
     }
   }
   moe_expert_table* t = new moe_expert_table();
@@ -204,14 +222,18 @@ int moe_expert_table_create(const void* const* packed, const void* const* scales
   t->K = K;
   t->device = current_device();
   t->d_maps = nullptr;
+  t->d_maps64 = nullptr;
   t->d_packed = nullptr;
   t->d_scales = nullptr;
   t->d_scale2 = nullptr;
   bool ok = cudaMalloc(&t->d_maps, maps.size() * sizeof(CUtensorMap)) == cudaSuccess &&
+            cudaMalloc(&t->d_maps64, maps64.size() * sizeof(CUtensorMap)) == cudaSuccess &&
             cudaMalloc(&t->d_packed, (size_t)E * sizeof(void*)) == cudaSuccess &&
             cudaMalloc(&t->d_scales, (size_t)E * sizeof(void*)) == cudaSuccess &&
             cudaMalloc(&t->d_scale2, (size_t)E * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok &&
+       cudaMemcpy(t->d_maps64, maps64.data(), maps64.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_packed, packed, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_scales, scales, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(t->d_scale2, scale2, (size_t)E * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
@@ -227,6 +249,7 @@ int moe_expert_table_destroy(moe_expert_table* t) {
   if (t == nullptr) return MOE_OK;
   cudaDeviceSynchronize();
   cudaFree(t->d_maps);
+  cudaFree(t->d_maps64);
   cudaFree(t->d_packed);
   cudaFree(t->d_scales);
   cudaFree(t->d_scale2);
@@ -325,10 +348,13 @@ int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t*
 
 // swiglu_half = 0: plain GEMM into C [R, ldc >= N]; otherwise the fused SwiGLU epilogue with
 // I = swiglu_half = N / 2 writing BF16 act [R, ldc >= I].
+// tiles_per_row (out, optional): how many CTA tiles of this launch cover one output row (the
+// producer side of the forward's GEMM overlap)
 static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids, const moe_expert_table* W,
                         const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st,
                         int swiglu_half = 0, float limit = 0.f, int* ready_out = nullptr,
-                        const int* ready_in = nullptr, int ready_need = 0, int* tile_counter = nullptr) {
+                        const int* ready_in = nullptr, int ready_need = 0, int* tile_counter = nullptr,
+                        int* tiles_per_row = nullptr) {
   if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
   if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (swiglu_half && (c_dtype != MOE_DTYPE_BF16 || W->N != 2 * swiglu_half || swiglu_half % 128 != 0))
@@ -361,6 +387,19 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.ready_in = ready_in;
   a.ready_need = ready_need;
   a.tile_counter = tile_counter;
+  a.wmaps64 = W->d_maps64;
+  a.A = A;
+  a.lda = lda;
+  a.wait_ns = gemm_wait_limit_ns();
+  const int mode = g_gemm_kernel.load(std::memory_order_relaxed);
+  const bool pair = mode != MOE_GEMM_KERNEL_SINGLE && pair_gemm_supported(a);
+  if (mode == MOE_GEMM_KERNEL_PAIR && !pair) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // CTA tiles of this launch covering one output row: the producer side of the forward's GEMM
+  // overlap publishes per tile (and, for absent experts' zero rows, this many per row)
+  const int tiles = pair ? 2 * (W->N / 256) : (W->N + 255) / 256;
+  if (tiles_per_row) *tiles_per_row = tiles;
+  if (ready_out != nullptr) a.ready_need = tiles;
+  if (pair) return pair_gemm_launch(a, st);
   return grouped_gemm_launch(a, A, a_rows, lda, st);
 }
 
@@ -517,6 +556,7 @@ int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspac
   L->act = take(R * I * 2);
   L->Y = take(R * H * 2);
   L->x_stage = take(T * H * 2);
+  L->x_sorted = take(R * H * 2);
   L->total = o;
   return MOE_OK;
 }
@@ -609,7 +649,13 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   const bool overlap = !small && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   int32_t* ready = overlap ? reinterpret_cast<int32_t*>(base + L.ready) : nullptr;
+  int producer_tiles = 0;
   if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, E + 1)) != MOE_OK) return rc;
+  // the fused gate/up GEMM on CTA pairs reads its token rows in expert order
+  const bool pair_gu = overlap && g_gemm_kernel.load(std::memory_order_relaxed) != MOE_GEMM_KERNEL_SINGLE &&
+                       pair_gemm_shape_ok(2 * I, H, E, I);
+  uint16_t* x_sorted = reinterpret_cast<uint16_t*>(base + L.x_sorted);
+  if (pair_gu && (rc = gather_rows_launch(xg, T, H, sti, off, E, R, H, x_sorted, err, st)) != MOE_OK) return rc;
   ev(3);
   // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
   if (small) {
@@ -620,17 +666,25 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     if ((rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
+  } else if (pair_gu) {
+    // CTA-pair kernel: the gathered token rows are first copied into expert order (x_sorted), so
+    // the GEMM loads contiguous rows with tiled TMA boxes
+    rc = gemm_checked(x_sorted, R, H, nullptr, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit,
+                      ready, nullptr, 0, nullptr, &producer_tiles);
+    if (rc != MOE_OK) return rc;
+    ev(4);
   } else {
-    // one producer CTA tile per 128 activation columns (a gate block and its up block)
+    // the gate/up launch reports how many of its CTA tiles cover one activation row (single-CTA
+    // kernel: one per 128 activation columns; CTA pairs: two per 128)
     rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit, ready,
-                      nullptr, I / 128);
+                      nullptr, 0, nullptr, &producer_tiles);
     if (rc != MOE_OK) return rc;
     ev(4);
   }
   ev(5);
   rc = small ? gemv_checked(act, R, I, nullptr, w_down, off, R, Y, H, 0, 0.f, st)
              : gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st, 0, 0.f, nullptr, ready,
-                            I / 128, ready ? ready + E : nullptr);
+                            producer_tiles, ready ? ready + E : nullptr);
   if (rc != MOE_OK) return rc;
   ev(6);
   if (shared_ready && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(shared_ready), 0) != cudaSuccess)
@@ -638,6 +692,29 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   if ((rc = combine_launch(Y, t2p, wts, shared_out, T, k, H, out, st)) != MOE_OK) return rc;
   ev(7);
   return MOE_OK;
+}
+
+// ------------------------------------------------------------------------------------------ debug
+
+int moe_debug_set_gemm_kernel(int which) {
+  if (which != MOE_GEMM_KERNEL_AUTO && which != MOE_GEMM_KERNEL_SINGLE && which != MOE_GEMM_KERNEL_PAIR)
+    return MOE_ERR_INVALID_ARG;
+  g_gemm_kernel.store(which, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+int moe_debug_grouped_gemm_after(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
+                                 const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
+                                 int c_dtype, const int32_t* ready, int ready_need, void* stream) {
+  if (ready == nullptr || ready_need < 1) return MOE_ERR_INVALID_ARG;
+  return gemm_checked(A, a_rows, lda, gather_ids, W, expert_offsets, R, C, ldc, c_dtype, as_stream(stream), 0, 0.f,
+                      nullptr, ready, ready_need, nullptr);
+}
+
+unsigned long long moe_debug_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) ns = 2000000000ull;
+  if (ns > 2000000000ull) ns = 2000000000ull;
+  return g_wait_limit_ns.exchange(ns, std::memory_order_relaxed);
 }
 
 // ------------------------------------------------------------------------------------------ errors

@@ -12,7 +12,11 @@ namespace moe {
 // Arguments of the grouped W4A16 GEMM kernel (the activation tensor map is passed separately as
 // a __grid_constant__ parameter).
 struct GemmArgs {
-  const CUtensorMap* wmaps;   // device [E][2]: packed [N, K/2] map, scales [N, K/16] map
+  const CUtensorMap* wmaps;   // device [E][2]: packed [N, K/2] map, scales [N, K/16] map (128-row boxes)
+  const CUtensorMap* wmaps64; // device [E][2]: the same maps with 64-row boxes (CTA-pair kernel)
+  const void* A;              // activations (BF16, row stride lda elements); the pair kernel reads them directly
+  int lda;
+  uint64_t wait_ns;           // bound of every pipeline wait of the CTA-pair kernel
   const void* const* packed;  // device [E]: packed pointers (NULL = absent expert)
   const float* scale2;        // device [E]
   const int32_t* gather;      // device [R] or NULL (identity)
@@ -46,6 +50,17 @@ int device_sm_count();
 int* device_error_word();  // device address of the current device's error word
 
 int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda, cudaStream_t stream);
+// The CTA-pair kernel (pair_gemm.cu): N a multiple of 256 (gate/up with the fused SwiGLU: N = 2I,
+// I a multiple of 128), K a multiple of 256, 64-row weight maps present.
+bool pair_gemm_supported(const GemmArgs& args);
+bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half);
+// token rows in expert order (the pair GEMM's contiguous A): xs[p] = x[sorted_token_ids[p]], p <
+// expert_offsets[E]
+int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
+                       const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st);
+int pair_gemm_launch(const GemmArgs& args, cudaStream_t stream);
+// Bound of the pipeline waits of the GEMM kernels (2 s; a debug entry point may lower it).
+uint64_t gemm_wait_limit_ns();
 
 // Launch with programmatic stream serialization (the kernel calls griddep_wait() before it reads
 // what earlier work in the stream wrote).

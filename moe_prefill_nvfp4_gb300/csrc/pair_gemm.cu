@@ -1,0 +1,705 @@
+// pair_gemm.cu -- grouped W4A16 GEMM on CTA pairs (tcgen05.mma.cta_group::2) for sm_103a.
+//
+// One launch covers every expert ("Module forward_prefill_gemm", "What this replaces": one launch
+// for all experts over an expert_offsets prefix sum, the A gather through sorted_token_ids inside
+// the kernel).  For each expert e and sorted row p in [off[e], off[e+1]):
+//     C[p, n] = sum_k A[g(p), k] * Wdq_e[n, k],   Wdq = bf16(fp32(E2M1 * E4M3) * scale2).
+//
+// Work decomposition ("swap AB", as in the single-CTA kernel): the weight rows are the MMA's M
+// operand, the expert's token rows its N operand.  Two CTAs of a cluster form a pair whose MMA has
+// M = 256: each CTA dequantises its own 128 weight rows into its TENSOR MEMORY (tcgen05.st), each
+// holds half of the token tile (N/2 rows of B) in its shared memory, and one thread of the even CTA
+// issues the pair's MMAs; both CTAs' TMEM receive their 128 rows x N of the FP32 accumulator.  A
+// tile is (expert, 256 weight rows, up to BN token rows); with BN = 256 each MMA instruction does
+// four times the work of a 128 x 128 one, which is what keeps the tensor pipe busy: one thread
+// issues an MMA only every ~70-120 cycles, and the dequantising warps on its sub-partition make
+// it slower, so small MMAs leave the tensor pipe idle.
+//
+// B rows are contiguous: the down GEMM's activation rows are already in expert order, and the
+// forward copies the gate/up GEMM's gathered token rows into expert order first (one copy kernel;
+// a TMA gather4 moves only ~12 B/cycle per SM and a 256-token tile needs ~32 B/cycle, 16-byte
+// cp.async gathers from two warps measured ~8 B/cycle).  Each CTA loads the rows it holds with
+// tiled TMA boxes (16 rows x 64 k, 128-byte swizzle) whose transaction bytes complete on the even
+// CTA's barrier (the .cta_group::2 form).  There is no cluster multicast.
+//
+// Warp roles (16 warps):
+//   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global
+//   4-7   dequantisation (8-11 a second warpgroup taking alternate atoms when NDQ = 2)
+//   12    weight producer (TMA: packed 2 x [64 rows x 128 B] swizzled + scales 2 x [64 x 16 B])
+//   13    B producer (TMA: this CTA's half of the token tile)
+//   14    MMA issuer (even CTA, one thread); TMEM allocation in both CTAs
+// Per atom (64 k) the even CTA's "full" barrier collects the 4 dequantising warps of each CTA (the
+// odd CTA's arrive remotely), the even CTA's B producer (arrival with the expected bytes of both
+// CTAs' boxes) and both CTAs' TMA transaction bytes; one multicast commit then releases the
+// atom's B and A slots in both CTAs.
+// The gate/up projection with the fused SwiGLU maps each CTA's 128 rows as 64 gate rows + the 64
+// matching up rows, interleaved in 16-row groups so that each warp of the epilogue holds a gate
+// row and its up row in lanes l and l + 16 of the same warp.
+//
+// Every pipeline wait is bounded (GemmArgs::wait_ns): on a timeout the CTA records
+// MOE_DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and returns.
+
+#include <algorithm>
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace pg {
+
+constexpr int BM = 128;          // weight rows per CTA (TMEM lanes); the pair's MMA has M = 256
+constexpr int PAIR_ROWS = 256;
+constexpr int BKW = 256;         // k per weight stage (128 packed bytes per row)
+constexpr int BKA = 64;          // k per atom: one B stage, one TMEM A stage, four MMAs
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_WARPS = 16;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int WARP_WP = 12, WARP_BP = 13, WARP_MMA = 14;
+constexpr int MAX_E = 512;
+
+// BN: token-tile width (the pair's MMA N, <= 256, each CTA holds BN/2 rows of B); ND:
+// accumulator buffers (2 lets the epilogue of one tile overlap the next tile's MMAs); NDQ:
+// dequantising warpgroups.  TMEM: ND*BN accumulator columns, then NS A stages of 32 columns.
+template <int BN_, int ND_, int NDQ_>
+struct Cfg {
+  static constexpr int BN = BN_;
+  static constexpr int ND = ND_;
+  static constexpr int NDQ = NDQ_;
+  static constexpr int BH = BN / 2;
+  static constexpr int A_COL = ND * BN;
+  static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A stages = B stages
+  static constexpr int NW = 3;
+  static constexpr int B_STAGE = BH * 128;
+  static constexpr int PK_STAGE = BM * 128;
+  static constexpr int SC_STAGE = BM * 16;
+  static constexpr int EPI_WARP_BYTES = 32 * 32 * 4;
+  static constexpr int OFF_B = 0;
+  static constexpr int OFF_PK = OFF_B + NS * B_STAGE;
+  static constexpr int OFF_SC = OFF_PK + NW * PK_STAGE;
+  static constexpr int OFF_EPI = OFF_SC + NW * SC_STAGE;
+  static constexpr int OFF_OFFS = OFF_EPI + 4 * EPI_WARP_BYTES;
+  static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
+  static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
+  // barriers: full[NS] empty[NS] w_full[NW] w_empty[NW] d_full[ND] d_empty[ND] drain
+  static constexpr int NBAR = 2 * NS + 2 * NW + 2 * ND + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 32;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;
+  static constexpr int FULL_COUNT = 2 * 4 + 1;  // dequantising warps of both CTAs + the B producer
+  static_assert(BN % 32 == 0 && BN <= 256 && NS >= 2, "token tile / TMEM columns");
+  static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
+  static_assert(BYTES + 1024 <= 232448, "shared memory");
+  static_assert(NDQ == 1 || NDQ == 2, "dequantising warpgroups");
+};
+
+struct Tile {
+  int e, ng, p0, cnt, bn;
+};
+
+// Tile g -> (expert, n-group of 256 weight rows, token rows).  Expert e owns tiles
+// [tbase[e], tbase[e+1]): ntt token tiles x NG n-groups, n-group fastest, so the pairs running at
+// the same time share token rows (and the expert's weights) in L2.  bn: the token count rounded up
+// to 32 (each CTA then loads whole 16-row boxes).
+template <int BN>
+MOE_DEV Tile decode(int g, const int* tbase, const int* offs, int E, int NG) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tbase[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  Tile t;
+  t.e = lo;
+  const int m = offs[lo + 1] - offs[lo];
+  const int ntt = (m + BN - 1) / BN;
+  const int local = g - tbase[lo];
+  const int tt = local / NG;
+  t.ng = local - tt * NG;
+  const int chunk = (((m + ntt - 1) / ntt) + 31) & ~31;
+  t.p0 = offs[lo] + tt * chunk;
+  t.cnt = min(chunk, m - tt * chunk);
+  t.bn = (t.cnt + 31) & ~31;
+  return t;
+}
+
+// ------------------------------------------------------------------------- bounded waits
+
+MOE_DEV bool wait_local(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// for barriers that CTAs of the cluster arrive on remotely (acquire at cluster scope)
+MOE_DEV bool wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+MOE_DEV bool warp_wait_local(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
+  bool ok = true;
+  if (lane_id() == 0) ok = wait_local(bar, parity, abort_flag, err, limit);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+MOE_DEV bool wait_counter(const int* p, int need, volatile int* abort_flag, int* err, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit) {
+      *abort_flag = 1;
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
+// Arrive on the barrier at offset `bar` of the even CTA (local when this is the even CTA).  The
+// remote arrive keeps the instruction's default semantics (release at CTA scope): the data it
+// publishes is tensor memory written by tcgen05.st, ordered by the tcgen05 fences around the
+// barrier, not generic memory (a release at cluster scope cost ~0.5 us per arrive here).
+MOE_DEV void arrive_leader(uint32_t bar, uint32_t rank) {
+  if (rank == 0) {
+    mbar_arrive(bar);
+  } else {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(bar), "r"(0));
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+  }
+}
+
+// Address of the barrier at offset `bar` in the even CTA, in the shared::cluster window.
+MOE_DEV uint32_t leader_addr(uint32_t bar) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(bar), "r"(0));
+  return ra;
+}
+
+// Tiled 2D TMA load into this CTA's shared memory whose transaction bytes complete on `bar`, a
+// barrier of either CTA of the pair (shared::cluster address).
+MOE_DEV void tma_load_2d_pair(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------- tcgen05, pair form
+
+MOE_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+MOE_DEV void tmem_relinquish_pair() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;"); }
+MOE_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// One 64-k atom on the pair: four k16 MMAs, A (256 rows: 128 in each CTA's TMEM) advancing 8
+// columns per step, B (N rows: the first N/2 in the even CTA's shared memory, the rest at the
+// same offset in the odd CTA's) advancing 32 bytes (+2 in the descriptor's address field).
+MOE_DEV void mma4_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 b1, b2, b3;\n .reg .b32 a1, a2, a3;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+      " add.s64 b1, %2, 2;\n add.s64 b2, %2, 4;\n add.s64 b3, %2, 6;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], b1, %3, q;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], b2, %3, q;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], b3, %3, q;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the barrier at offset `bar` in both CTAs of the pair when every tcgen05 op issued
+// so far by this thread has completed.
+MOE_DEV void commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+template <class C>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    pair_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  int* s_offs = reinterpret_cast<int*>(smem + C::OFF_OFFS);
+  int* s_tbase = reinterpret_cast<int*>(smem + C::OFF_TBASE);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  constexpr int NS = C::NS, NW = C::NW, ND = C::ND;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (NS + s); };
+  auto w_full = [&](int s) { return bar0 + 8u * (2 * NS + s); };
+  auto w_empty = [&](int s) { return bar0 + 8u * (2 * NS + NW + s); };
+  auto d_full = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NW + d); };
+  auto d_empty = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NW + ND + d); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * NS + 2 * NW + 2 * ND);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* s_bad = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = args.E;
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+  const int pid = (int)cluster_id_x();
+  const int npairs = (int)cluster_count_x();
+  const uint64_t limit = args.wait_ns;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full(s), C::FULL_COUNT);
+      mbar_init(empty(s), 1);
+    }
+    for (int s = 0; s < NW; ++s) {
+      mbar_init(w_full(s), 1);
+      mbar_init(w_empty(s), 4 * C::NDQ);
+    }
+    for (int d = 0; d < ND; ++d) {
+      mbar_init(d_full(d), 1);
+      mbar_init(d_empty(d), 8);  // the 4 epilogue warps of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc_pair(smem_u32(s_tmem), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  // everything above overlaps the previous kernel of the stream; its outputs are read below (a
+  // consumer of a producer GEMM's per-expert counters waits per expert instead, and for the whole
+  // producer grid at its end)
+  if (args.ready_in == nullptr) griddep_wait();
+  griddep_launch_dependents();
+  for (int i = tid; i <= E; i += NUM_THREADS) s_offs[i] = args.offsets[i];
+  __syncthreads();
+
+  const int NG = args.N / PAIR_ROWS;  // n-groups of 256 weight rows (gate/up: 128 act columns)
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int sum = 0;
+    bool bad = false;
+    for (int e = e0; e < e1; ++e) {
+      const int m = s_offs[e + 1] - s_offs[e];
+      if (m < 0) bad = true;
+      if (m > 0 && args.packed[e] != nullptr) sum += NG * ((m + C::BN - 1) / C::BN);
+    }
+    if (lane == 0 && (s_offs[0] != 0 || s_offs[E] > args.R || s_offs[E] < 0)) bad = true;
+    bad = __any_sync(0xffffffffu, bad);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      s_tbase[e] = bad ? 0 : run;
+      const int m = s_offs[e + 1] - s_offs[e];
+      if (m > 0 && args.packed[e] != nullptr) run += NG * ((m + C::BN - 1) / C::BN);
+    }
+    if (lane == 31) s_tbase[E] = bad ? 0 : incl;
+    if (lane == 0) *s_bad = bad ? 1 : 0;
+    if (bad && lane == 0 && blockIdx.x == 0) set_error(args.err, MOE_DEVERR_BAD_OFFSETS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = s_tbase[E];
+  const int KA = args.K / BKA;
+  const int KW = args.K / BKW;
+  const int half = args.swiglu_half;
+  // the tiles of this pair: pid, pid + npairs, ... (both CTAs walk the same list)
+  auto tile_at = [&](int i) -> int {
+    const int g = pid + i * npairs;
+    return g < total ? g : -1;
+  };
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp;
+    uint8_t* stg = smem + C::OFF_EPI + q * C::EPI_WARP_BYTES;
+    const bool f32 = args.c_dtype == MOE_DTYPE_F32;
+    const int esz = f32 ? 4 : 2;
+    const int out_cols = half ? half : args.N;
+    if (!*s_bad) {
+      // rows of absent experts are written as zeros (the pages' zeroed routed-output rows)
+      const int chunks_per_row = out_cols * esz / 16;
+      for (int e = 0; e < E; ++e) {
+        if (args.packed[e] != nullptr) continue;
+        int nz = 0;
+        for (int r = s_offs[e] + blockIdx.x; r < s_offs[e + 1]; r += gridDim.x, ++nz) {
+          uint8_t* row = reinterpret_cast<uint8_t*>(args.C) + (size_t)r * args.ldc * esz;
+          for (int c = tid; c < chunks_per_row; c += 128) *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        if (args.ready_out != nullptr && nz > 0) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) counter_add_release(args.ready_out + e, nz * args.ready_need);
+        }
+      }
+    }
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    for (int it = 0;; ++it) {
+      const int g = tile_at(it);
+      if (g < 0) break;
+      const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
+      const int db = it % ND;
+      if (!warp_wait_local(d_full(db), (it / ND) & 1, s_abort, args.err, limit)) break;
+      tc_fence_after();
+      const uint32_t dcol = (uint32_t)(db * C::BN);
+      if (half) {
+        // fused clamped SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
+        // act column a0 + (lane & 15); act = silu(min(g, L)) * clamp(u, -L, L) from the FP32
+        // accumulators (not rounded to BF16 first: against the stage-rounding reference that
+        // keeps each element within half a BF16 unit of g and u), rounded to BF16
+        const int a0 = t.ng * 128 + (int)rank * 64 + q * 16;
+        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+        const bool is_gate = lane < 16;
+        for (int c0 = 0; c0 < t.cnt; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(lane_base + dcol + c0, v);
+          tmem_wait_ld();
+          if (c0 + 32 >= t.cnt) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_leader(d_empty(db), rank);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            // lane l < 16 keeps tokens j (its g, the partner's u); lane l + 16 tokens 16 + j
+            const float mine = __uint_as_float(is_gate ? v[j] : v[16 + j]);
+            const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(is_gate ? v[16 + j] : v[j]), 16);
+            const float gv = is_gate ? mine : other;
+            const float uv = is_gate ? other : mine;
+            const int tok = is_gate ? j : 16 + j;
+            st[tok * 16 + (lane & 15)] = __float2bfloat16_rn(swiglu_clamped(gv, uv, args.limit));
+          }
+          __syncwarp();
+          const int rows = min(32, t.cnt - c0);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = lane + 32 * i;
+            const int r = c >> 1, h = c & 1;
+            if (r < rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 + h * 16);
+              uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + (size_t)(t.p0 + c0 + r) * args.ldc + a0 + h * 8;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+          __syncwarp();
+        }
+      } else {
+        const int n0 = t.ng * PAIR_ROWS + (int)rank * BM + q * 32;
+        for (int c0 = 0; c0 < t.cnt; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(lane_base + dcol + c0, v);
+          tmem_wait_ld();
+          if (c0 + 32 >= t.cnt) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_leader(d_empty(db), rank);
+          }
+          __syncwarp();
+          if (f32) {
+            float* s = reinterpret_cast<float*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __uint_as_float(v[j]);
+          } else {
+            __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          }
+          __syncwarp();
+          const int rows = min(32, t.cnt - c0);
+          const int cpr = 32 * esz / 16;  // 16-byte chunks per staged row (4 bf16, 8 f32)
+          for (int c = lane; c < 32 * cpr; c += 32) {
+            const int r = c / cpr, cc = c - r * cpr;
+            if (r < rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 * esz + cc * 16);
+              uint8_t* dst = reinterpret_cast<uint8_t*>(args.C) +
+                             ((size_t)(t.p0 + c0 + r) * args.ldc + n0 + cc * (16 / esz)) * esz;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      if (args.ready_out != nullptr) {  // this warp's part of the tile's rows is stored
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) counter_add_release(args.ready_out + t.e, t.cnt);
+      }
+    }
+  } else if (warp < 4 + 4 * C::NDQ) {
+    // ------------------------------------------------------------------ dequantisation
+    // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
+    // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
+    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes the atoms ai with ai % NDQ == wg.
+    const int wg = (warp - 4) >> 2;
+    const int q = warp & 3;
+    const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int ai = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int g = tile_at(it);
+      if (g < 0) break;
+      const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
+      const float s2 = args.scale2[t.e];
+      for (int kb = 0; kb < KA; ++kb, ++ai) {
+        if (C::NDQ == 2 && (ai & 1) != wg) continue;
+        const int wi = ai >> 2;  // weight stage (4 atoms)
+        const int ws = wi % NW;
+        const int atom = ai & 3;
+        if (atom == (C::NDQ == 2 ? wg : 0) && !warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* pk = smem + C::OFF_PK + ws * C::PK_STAGE + sr * 128;
+        const uint4 lo = *reinterpret_cast<const uint4*>(pk + (((2 * atom) ^ (sr & 7)) << 4));
+        const uint4 hi = *reinterpret_cast<const uint4*>(pk + (((2 * atom + 1) ^ (sr & 7)) << 4));
+        const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16 + atom * 4);
+        if (atom == 4 - C::NDQ + wg) {  // this warp's last read of the weight stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(w_empty(ws));
+        }
+        const int s = ai % NS;
+        if (!warp_wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        uint32_t out[32];
+        dequant64(w, sc, s2, out);
+        tmem_st_32x32b_x32(tmem_base + lane_addr + C::A_COL + s * 32, out);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(full(s), rank);
+      }
+    }
+  } else if (warp == WARP_WP) {
+    // ------------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int wi = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int g = tile_at(it);
+        if (g < 0) break;
+        const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
+        const CUtensorMap* mp = args.wmaps64 + 2 * t.e;
+        const CUtensorMap* ms = mp + 1;
+        prefetch_tmap(mp);
+        prefetch_tmap(ms);
+        // this CTA's 128 weight rows as two 64-row boxes
+        const int r0 = half ? t.ng * 128 + (int)rank * 64 : t.ng * PAIR_ROWS + (int)rank * BM;
+        const int r1 = half ? half + r0 : r0 + 64;
+        for (int ks = 0; ks < KW; ++ks, ++wi) {
+          const int s = wi % NW;
+          if (!wait_local(w_empty(s), ((wi / NW) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(w_full(s), C::PK_STAGE + C::SC_STAGE);
+          const uint32_t pk = sbase + C::OFF_PK + s * C::PK_STAGE;
+          const uint32_t sc = sbase + C::OFF_SC + s * C::SC_STAGE;
+          tma_load_2d(pk, mp, ks * 128, r0, w_full(s));
+          tma_load_2d(pk + 64 * 128, mp, ks * 128, r1, w_full(s));
+          tma_load_2d(sc, ms, ks * 16, r0, w_full(s));
+          tma_load_2d(sc + 64 * 16, ms, ks * 16, r1, w_full(s));
+        }
+      }
+      if (!ok)
+        for (int j = max(0, wi - NW); j < wi; ++j) mbar_wait_drain(w_full(j % NW), (j / NW) & 1);
+    }
+  } else if (warp == WARP_BP) {
+    // ------------------------------------------------------------------ B producer
+    // Both CTAs: for each atom, this CTA's rows [p0 + rank*bn/2, p0 + (rank+1)*bn/2) of the tile,
+    // k [64 kb, 64 kb + 64), as 16-row tiled boxes whose bytes complete on the even CTA's full
+    // barrier; the even CTA's thread arrives there with the bytes of both CTAs' boxes.  Rows past
+    // the tile's count belong to the next expert (or lie past the tensor and are zero-filled): the
+    // MMA reads them into accumulator columns the epilogue never stores.
+    if (lane == 0) {
+      int ai = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int g = tile_at(it);
+        if (g < 0) break;
+        const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
+        const int nrows = t.bn >> 1;  // a multiple of 16
+        const int y0 = t.p0 + (int)rank * nrows;
+        if (args.ready_in != nullptr) {
+          // the producer GEMM has stored every row of this expert (all its CTA tiles' epilogue warps)
+          if (!wait_counter(args.ready_in + t.e, (s_offs[t.e + 1] - s_offs[t.e]) * args.ready_need * 4, s_abort,
+                            args.err, limit)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        for (int kb = 0; kb < KA; ++kb, ++ai) {
+          const int s = ai % NS;
+          if (!wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(full(s), 2u * (uint32_t)nrows * 128u);
+          const uint32_t bar = leader_addr(full(s));
+          const uint32_t dst0 = sbase + C::OFF_B + s * C::B_STAGE;
+          for (int j = 0; j < nrows; j += 16) tma_load_2d_pair(dst0 + j * 128, &bmap, kb * BKA, y0 + j, bar);
+        }
+      }
+      if (!ok) {
+        // let this CTA's copies land before it leaves: its last NS atoms' boxes complete on the
+        // even CTA's barriers, which both CTAs keep alive until the final cluster barrier
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int ai = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int g = tile_at(it);
+        if (g < 0) break;
+        const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
+        const int db = it % ND;
+        if (!wait_cluster(d_empty(db), ((it / ND) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t idesc = make_idesc_bf16(PAIR_ROWS, t.bn);
+        const uint64_t bdesc0 = make_sdesc_sw128(sbase + C::OFF_B);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(db * C::BN);
+        for (int kb = 0; kb < KA; ++kb, ++ai) {
+          const int s = ai % NS;
+          if (!wait_cluster(full(s), (ai / NS) & 1, s_abort, args.err, limit)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bdesc = bdesc0 + (uint64_t)((s * C::B_STAGE) >> 4);
+          mma4_pair(d_tmem, tmem_base + C::A_COL + s * 32, bdesc, idesc, kb != 0);
+          commit_pair(empty(s));
+        }
+        if (ok) commit_pair(d_full(db));
+      }
+      if (!ok) {  // let every issued MMA finish before TMEM is freed
+        commit_pair(drain_bar);
+        mbar_wait_drain(drain_bar, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA frees TMEM or leaves while its peer may still signal it
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+  // a consumer completes only after its producer grid (stream order for the launches after it)
+  if (args.ready_in != nullptr) griddep_wait();
+}
+
+using CfgWide = Cfg<256, 1, 2>;   // 256-token tiles, one accumulator
+using CfgPair = Cfg<128, 2, 2>;   // 128-token tiles, two accumulator buffers
+
+template <class C>
+int launch_cfg(const CUtensorMap& bmap, const GemmArgs& args, cudaStream_t stream) {
+  static std::atomic<int> configured[64];
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(pair_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured[dev].store(1, std::memory_order_release);
+  }
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = max_clusters[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    cfg.gridDim = dim3(nsm);
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+    max_clusters[dev].store(n, std::memory_order_relaxed);
+  }
+  // upper bound of the tiles: every expert's token tiles times the n-groups
+  const long long ng = args.N / PAIR_ROWS;
+  const long long max_tiles = ng * ((long long)args.E + (args.R + C::BN - 1) / C::BN);
+  const int npairs = (int)std::max<long long>(1, std::min<long long>(n, max_tiles));
+  cfg.gridDim = dim3(2 * npairs);
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, pair_gemm_kernel<C>, bmap, args) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace pg
+
+bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half) {
+  return N % pg::PAIR_ROWS == 0 && K % pg::BKW == 0 && E <= pg::MAX_E && (swiglu_half == 0 || swiglu_half * 2 == N);
+}
+
+bool pair_gemm_supported(const GemmArgs& args) {
+  return args.wmaps64 != nullptr && args.gather == nullptr && pair_gemm_shape_ok(args.N, args.K, args.E, args.swiglu_half);
+}
+
+int pair_gemm_launch(const GemmArgs& args, cudaStream_t stream) {
+  if (!pair_gemm_supported(args)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap bmap;
+  {  // A rows (contiguous, expert order): boxes of 16 rows x 64 k, 128-byte swizzle
+    const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.a_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)args.lda * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)pg::BKA, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    const int rc = encode_tmap(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(args.A), dims, strides, box,
+                               estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != MOE_OK) return rc;
+  }
+  // token-tile width from the mean rows per expert (the distribution itself stays on the device)
+  const double mean_rows = (double)args.R / args.E;
+  if (mean_rows > 128.0) return pg::launch_cfg<pg::CfgWide>(bmap, args, stream);
+  return pg::launch_cfg<pg::CfgPair>(bmap, args, stream);
+}
+
+}  // namespace moe

@@ -662,6 +662,43 @@ int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, con
 }
 
 // ------------------------------------------------------------------------------------------------
+// token rows in expert order for the gate/up GEMM: xs[p, :] = x[sorted_token_ids[p], :] for the
+// sorted rows p < expert_offsets[E] (read on the device), 16-byte vectors, grid-stride.  A token id
+// outside [0, a_rows) records MOE_DEVERR_BAD_GATHER and copies row 0.
+
+constexpr int GATHER_THREADS = 256;
+
+__global__ void __launch_bounds__(GATHER_THREADS)
+    gather_rows_kernel(const uint16_t* __restrict__ x, int a_rows, int lda, const int32_t* __restrict__ sti,
+                       const int32_t* __restrict__ offsets, int E, int R, int H, uint16_t* __restrict__ xs, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int rows = min(max(__ldg(offsets + E), 0), R);
+  const int nvec = H / 8;
+  const int64_t total = (int64_t)rows * nvec;
+  for (int64_t g = (int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * GATHER_THREADS) {
+    const int p = (int)(g / nvec), v = (int)(g - (int64_t)p * nvec);
+    int tok = __ldg(sti + p);
+    if ((unsigned)tok >= (unsigned)a_rows) {
+      if (v == 0) set_error(err, MOE_DEVERR_BAD_GATHER);
+      tok = 0;
+    }
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * lda) + v);
+    *(reinterpret_cast<uint4*>(xs + (size_t)p * H) + v) = val;
+  }
+}
+
+int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
+                       const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st) {
+  const int nsm = device_sm_count();
+  const int64_t need = ((int64_t)R * (H / 8) + GATHER_THREADS - 1) / GATHER_THREADS;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)(nsm > 0 ? nsm : 148) * 8));
+  return launch_pdl(gather_rows_kernel, dim3(grid), dim3(GATHER_THREADS), 0, st, x, a_rows, lda, sorted_token_ids,
+                    expert_offsets, E, R, H, xs, err);
+}
+
+// ------------------------------------------------------------------------------------------------
 // standalone dequantisation: one thread per (row, 64-k chunk), the GEMM's dequant64 routine
 
 __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales, float s2, int N,

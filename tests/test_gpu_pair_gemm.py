@@ -1,0 +1,177 @@
+"""GPU parity of the CTA-pair grouped GEMM (tcgen05 cta_group::2) against the oracle.
+
+The pair kernel is the default wherever N % 256 == 0 and the A rows are contiguous (the forward
+copies the gate/up GEMM's gathered token rows into expert order first; a standalone call with
+gather_ids takes the single-CTA kernel).  These cases force it (``moe_debug_set_gemm_kernel``) on
+A rows in expert order and compare with the oracle's grouped GEMM on the same BF16 operands
+(FP32 output: only the FP32 summation order differs, so 2e-6 of max|ref|), with the exact
+special case bit for bit, and with the single-CTA kernel.  Shapes cover both tile configurations
+(128-token tiles with two accumulator buffers, 256-token tiles with one), ragged experts (1 row,
+32k + 1 rows, experts spanning several token tiles), absent and empty experts, and the fused
+SwiGLU.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import moe_prefill_nvfp4_gb300 as moe  # noqa: E402
+from oracle import moe_oracle as O  # noqa: E402
+from synth import inputs as S  # noqa: E402
+
+from gpu_helpers import TOL_BF16, bf16_dev, bf16_host, nerr, upload  # noqa: E402
+
+PAIR = moe.MOE_GEMM_KERNEL_PAIR
+SINGLE = moe.MOE_GEMM_KERNEL_SINGLE
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    moe.moe_get_device_error()
+    yield
+    moe.moe_debug_set_gemm_kernel(moe.MOE_GEMM_KERNEL_AUTO)
+    assert moe.moe_get_device_error() == 0
+
+
+def _run(c, which, c_dtype=torch.float32, identity=False, swiglu=False, guard=0):
+    """GPU sort + grouped GEMM with the chosen kernel.  `guard` extra rows and columns around the
+    output hold a sentinel that must survive."""
+    srt = moe.moe_sort_by_expert(torch.from_numpy(c.ids).cuda(), c.E)
+    proj = upload(c.w)
+    R = c.T * c.k
+    cols = c.N // 2 if swiglu else c.N
+    dt = torch.bfloat16 if swiglu else c_dtype
+    buf = torch.full((R + 2 * guard, cols + 8 * guard), 3.0, dtype=dt, device="cuda")
+    out = buf[guard:guard + R, :cols]
+    if identity or which == PAIR:  # the pair kernel reads A rows in expert order
+        A = bf16_dev(c.x)[srt["sorted_token_ids"].long()].contiguous()
+        gather = None
+    else:
+        A = bf16_dev(c.x)
+        gather = srt["sorted_token_ids"]
+    with moe.gemm_kernel(which):
+        if swiglu:
+            moe.moe_w4a16_grouped_gemm_swiglu(A, proj.table, srt["expert_offsets"], R, limit=7.0, gather_ids=gather,
+                                              out=out)
+        else:
+            moe.moe_w4a16_grouped_gemm(A, proj.table, srt["expert_offsets"], R, gather_ids=gather, out=out,
+                                       c_dtype=c_dtype)
+        torch.cuda.synchronize()
+    if guard:
+        g = buf.float()
+        assert (g[:guard] == 3.0).all() and (g[guard + R:] == 3.0).all() and (g[:, cols:] == 3.0).all(), "guard band"
+    proj.close()
+    return out, {k: v.cpu().numpy() for k, v in srt.items()}
+
+
+def _oracle(c, srt, variant="bf16"):
+    wfn = lambda e: None if c.w.packed[e] is None else O.dequant_nvfp4(c.w.packed[e], c.w.scales[e], c.w.scale2[e],
+                                                                     variant)
+    return O.grouped_gemm(O.bf16_bits_to_f64(c.x), srt["expert_offsets"], wfn, srt["sorted_token_ids"])
+
+
+def test_pair_exact_dyadic_bit_exact():
+    """Unit scales, scale2 = 1, integer activations: every product and partial sum is exact, so the
+    FP32 output equals the oracle bit for bit in any summation order."""
+    c = S.make_gemm_case(T=48, E=6, k=3, N=512, K=512, seed=121,
+                         x_sampler=lambda g, shp: g.integers(-2, 3, shp).astype(np.float32))
+    for e in range(c.E):
+        c.w.scales[e][:] = 0x38
+    c.w.scale2[:] = 1.0
+    C, srt = _run(c, PAIR)
+    np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), _oracle(c, srt))
+
+
+@pytest.mark.parametrize("T,E,k,N,K,identity", [
+    (40, 16, 8, 256, 512, False),      # ~20 rows per expert: 128-token tiles
+    (40, 16, 8, 512, 512, True),       # contiguous rows
+    (300, 24, 8, 768, 256, False),     # ~100 rows per expert, K = 256 (one weight stage)
+    (600, 4, 2, 512, 768, False),      # ~300 rows per expert: 256-token tiles, several per expert
+    (600, 4, 2, 256, 512, True),       # 256-token tiles, contiguous
+    (1030, 3, 1, 256, 512, False),     # ~343 rows, ragged 16k+6 tails
+], ids=["128tok-gathered", "128tok-contiguous", "100rows-K256", "256tok-gathered", "256tok-contiguous",
+        "256tok-ragged"])
+def test_pair_vs_oracle(T, E, k, N, K, identity):
+    c = S.make_gemm_case(T=T, E=E, k=k, N=N, K=K, seed=131 + T + N + K)
+    C, srt = _run(c, PAIR, identity=identity, guard=2)
+    assert nerr(C.cpu().numpy().astype(np.float64), _oracle(c, srt)) < 2e-6
+
+
+def test_pair_ragged_single_rows_absent_and_empty():
+    """Experts with 1, 2, 17 and 300+ rows, an absent expert (its rows zero), empty experts."""
+    g = np.random.default_rng(11)
+    T, E, k, N, K = 400, 9, 1, 256, 512
+    c = S.make_gemm_case(T=T, E=E, k=k, N=N, K=K, seed=141, absent=(4,))
+    ids = np.zeros((T, k), dtype=np.int32)
+    ids[:1] = 1
+    ids[1:3] = 2
+    ids[3:20] = 3
+    ids[20:40] = 4
+    ids[40:60] = 5
+    ids[60:] = 0  # 340 rows: two 256-token tiles at most
+    g.shuffle(ids)
+    c.ids = ids
+    C, srt = _run(c, PAIR, guard=1)
+    got = C.cpu().numpy().astype(np.float64)
+    o = srt["expert_offsets"]
+    assert o[5] > o[4] and (got[o[4]:o[5]] == 0).all()
+    assert nerr(got, _oracle(c, srt)) < 2e-6
+
+
+@pytest.mark.parametrize("c_dtype", [torch.float32, torch.bfloat16])
+def test_pair_equals_single_cta_kernel(c_dtype):
+    """Both kernels on the same operands: FP32 outputs within the summation-order difference,
+    BF16 outputs within one BF16 rounding."""
+    c = S.make_gemm_case(T=200, E=12, k=4, N=512, K=1024, seed=151)
+    a, _ = _run(c, PAIR, c_dtype=c_dtype)
+    b, _ = _run(c, SINGLE, c_dtype=c_dtype)
+    x, y = a.float().cpu().numpy().astype(np.float64), b.float().cpu().numpy().astype(np.float64)
+    assert nerr(x, y) < (2e-6 if c_dtype == torch.float32 else 2.0 ** -8)
+
+
+@pytest.mark.parametrize("T,E,k,I,big,identity", [(40, 16, 8, 256, False, False), (300, 24, 8, 256, True, False),
+                                                  (600, 4, 2, 128, True, False), (90, 12, 4, 768, False, True)],
+                         ids=["128tok", "100rows-clamped", "256tok-clamped", "identity"])
+def test_pair_swiglu_fused(T, E, k, I, big, identity):
+    """Gate/up GEMM with the clamped SwiGLU in the epilogue, act = silu(min(g, L)) * clamp(u, -L, L)
+    on the FP32 accumulators (the fused path has no BF16 G stage), against the oracle's SwiGLU of
+    its unrounded G; and within one BF16 unit of g and of u of the SwiGLU of the oracle's
+    BF16-rounded G.  `big` scales scale2 so that both clamps act."""
+    c = S.make_gemm_case(T=T, E=E, k=k, N=2 * I, K=512, seed=161 + T + I, absent=(1,))
+    if big:
+        c.w.scale2[:] = c.w.scale2 * 200.0
+    act, srt = _run(c, PAIR, identity=identity, swiglu=True, guard=1)
+    G64 = _oracle(c, srt)
+    G = O.round_to_bf16(G64.astype(np.float32)).astype(np.float64)
+    ref = O.swiglu_clamp(G[:, :I], G[:, I:], 7.0)
+    got = bf16_host(act)
+    if big:
+        assert (np.abs(G[:, :I]) > 7.0).mean() > 0.05 and (np.abs(G[:, I:]) > 7.0).mean() > 0.05
+    o = srt["expert_offsets"]
+    assert (got[o[1]:o[2]] == 0).all()
+    # per element against the SwiGLU of the unrounded G: the BF16 rounding of act (<= 2^-9
+    # relative) plus the FP32 summation-order difference of g and u carried through the SwiGLU
+    ref64 = O.swiglu_clamp(G64[:, :I], G64[:, I:], 7.0)
+    assert (np.abs(got - ref64) <= np.abs(ref64) * 2.0 ** -8 + 1e-4 * np.abs(ref64).max()).all()
+    assert nerr(got, ref64) < TOL_BF16
+    assert nerr(got, ref) < 2.0 ** -7
+
+
+def test_pair_refuses_gathered_rows():
+    """With gather_ids the pair kernel is not taken: PAIR mode refuses, AUTO takes the single-CTA
+    kernel."""
+    c = S.make_gemm_case(T=64, E=8, k=2, N=256, K=512, seed=171)
+    srt = moe.moe_sort_by_expert(torch.from_numpy(c.ids).cuda(), c.E)
+    proj = upload(c.w)
+    R = c.T * c.k
+    with moe.gemm_kernel(PAIR):
+        with pytest.raises(moe.MoeError):
+            moe.moe_w4a16_grouped_gemm(bf16_dev(c.x), proj.table, srt["expert_offsets"], R,
+                                       gather_ids=srt["sorted_token_ids"])
+    C = moe.moe_w4a16_grouped_gemm(bf16_dev(c.x), proj.table, srt["expert_offsets"], R,
+                                   gather_ids=srt["sorted_token_ids"], c_dtype=torch.float32)
+    s = {kk: v.cpu().numpy() for kk, v in srt.items()}
+    assert nerr(C.cpu().numpy().astype(np.float64), _oracle(c, s)) < 2e-6
+    proj.close()

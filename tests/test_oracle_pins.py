@@ -395,3 +395,28 @@ def test_shared_expert_joins_the_combine():
     without = O.prefill_forward(c, "bf16")
     np.testing.assert_allclose(with_shared["out64"], without["out64"] + with_shared["shared"], rtol=1e-12,
                                atol=1e-15)
+
+
+def test_pooled_expert_chain_equals_prefill_forward():
+    """The full-size GPU parity tests run the oracle's per-expert stages in worker processes
+    (tests/oracle_pool.py).  Split over experts and row blocks, the chain must be the oracle's
+    own prefill_forward in both variants, with an absent expert: equal up to the fp64 summation
+    order of the BLAS matmul (whose blocking depends on the row count), and equal to the bit
+    after each stage's rounding to FP32/BF16."""
+    from oracle_pool import OraclePool, run_block
+
+    c = S.make_block_case(T=50, H=256, I=128, E=7, k=3, routing="biased", seed=17, absent=(5,))
+    with OraclePool(2) as pool:
+        for variant in ("bf16", "exact"):
+            ref = O.prefill_forward(c, variant)
+            srt = {k: ref[k] for k in ("sorted_token_ids", "expert_offsets", "token_to_perm")}
+            got = run_block(pool, c, srt, variant, rows_per_task=7)
+            o = ref["expert_offsets"]
+            live = np.ones(int(o[-1]), dtype=bool)
+            live[o[5]:o[6]] = False  # the absent expert's rows stay zero in the oracle, NaN here
+            for key, stage in (("G64", "G"), ("act64", "act"), ("Y64", "Y")):
+                np.testing.assert_allclose(got[key][live], ref[key][live], rtol=1e-12, atol=0, err_msg=f"{variant} {key}")
+                np.testing.assert_array_equal(O._to_stage(got[key][live], variant), ref[stage][live])
+            Y = O._to_stage(np.where(np.isnan(got["Y64"]), 0.0, got["Y64"]), variant)
+            out = O.combine_indexed(Y, ref["token_to_perm"], ref["wts"])
+            np.testing.assert_array_equal(out, ref["out64"])

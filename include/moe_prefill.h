@@ -196,9 +196,10 @@ int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t
  * (metrale), swiglu_rows, applied to the gate/up product of the grouped-prefill arm):
  *   act[p, j] = silu(min(g, L)) * clamp(u, -L, L),  g = C[p, j], u = C[p, I + j], j < I,
  * with C the moe_w4a16_grouped_gemm product over a gate/up table of N = 2I rows (rows 0..I-1
- * gate, I..2I-1 up).  g and u are the FP32 accumulators (not rounded to BF16 first);
- * silu(z) = z / (1 + e^-z) in FP32; act is rounded to BF16 (nearest even).  The N x R
- * product never goes to memory.  Rows of absent experts are written as zeros.
+ * gate, I..2I-1 up).  g and u are the FP32 accumulators rounded to BF16 (nearest even), the
+ * values the pages' BF16 gate and up buffers hold ("glm5next_mlp/forward.rs" (spark),
+ * forward_dense: a_gate, a_up); silu(z) = z / (1 + e^-z) in FP32; act is rounded to BF16.  The
+ * N x R product never goes to memory.  Rows of absent experts are written as zeros.
  *   act          device BF16 [R, ld_act] (output), ld_act >= I, ld_act % 8 == 0
  * Other arguments as moe_w4a16_grouped_gemm.  Requires W->N = 2I with I % 128 == 0.
  */
@@ -379,11 +380,13 @@ int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_worksp
  * take effect for the launches issued after the call.
  *
  * moe_debug_set_gemm_kernel: which grouped GEMM kernel the GEMM entry points and the forward
- * launch.  MOE_GEMM_KERNEL_AUTO (the default) takes the CTA-pair kernel wherever its shapes
- * allow (N % 256 == 0; with the fused SwiGLU I % 128 == 0) and the single-CTA kernel otherwise;
- * SINGLE always takes the single-CTA kernel; PAIR makes the entry points return
- * MOE_ERR_UNSUPPORTED_SHAPE for shapes the pair kernel does not take.  Returns
- * MOE_ERR_INVALID_ARG for another value.
+ * launch.  MOE_GEMM_KERNEL_AUTO (the default) takes the CTA-pair kernel where it is faster
+ * (experts averaging more than 128 sorted rows) and its shapes allow it (N % 256 == 0; with the
+ * fused SwiGLU I % 128 == 0; A rows contiguous -- the forward copies the gate/up GEMM's gathered
+ * rows into expert order for it), and the single-CTA kernel otherwise; SINGLE always takes the
+ * single-CTA kernel; PAIR takes the pair kernel for every shape it allows and makes the entry
+ * points return MOE_ERR_UNSUPPORTED_SHAPE for the others.  Returns MOE_ERR_INVALID_ARG for
+ * another value.
  *
  * moe_debug_set_wait_limit_ns: the bound of every pipeline wait of the CTA-pair kernel
  * (default and maximum 2 s; 0 restores the default).  After the bound a waiting kernel records

@@ -392,7 +392,8 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.lda = lda;
   a.wait_ns = gemm_wait_limit_ns();
   const int mode = g_gemm_kernel.load(std::memory_order_relaxed);
-  const bool pair = mode != MOE_GEMM_KERNEL_SINGLE && pair_gemm_supported(a);
+  const bool pair = pair_gemm_supported(a) &&
+                    (mode == MOE_GEMM_KERNEL_PAIR || (mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, W->E)));
   if (mode == MOE_GEMM_KERNEL_PAIR && !pair) return MOE_ERR_UNSUPPORTED_SHAPE;
   // CTA tiles of this launch covering one output row: the producer side of the forward's GEMM
   // overlap publishes per tile (and, for absent experts' zero rows, this many per row)
@@ -652,8 +653,10 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   int producer_tiles = 0;
   if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, E + 1)) != MOE_OK) return rc;
   // the fused gate/up GEMM on CTA pairs reads its token rows in expert order
-  const bool pair_gu = overlap && g_gemm_kernel.load(std::memory_order_relaxed) != MOE_GEMM_KERNEL_SINGLE &&
-                       pair_gemm_shape_ok(2 * I, H, E, I);
+  const int gemm_mode = g_gemm_kernel.load(std::memory_order_relaxed);
+  const bool pair_gu = overlap && pair_gemm_shape_ok(2 * I, H, E, I) &&
+                       (gemm_mode == MOE_GEMM_KERNEL_PAIR ||
+                        (gemm_mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, E)));
   uint16_t* x_sorted = reinterpret_cast<uint16_t*>(base + L.x_sorted);
   if (pair_gu && (rc = gather_rows_launch(xg, T, H, sti, off, E, R, H, x_sorted, err, st)) != MOE_OK) return rc;
   ev(3);

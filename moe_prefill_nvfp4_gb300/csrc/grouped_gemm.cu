@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       if (C::NBLK == 2 && args.swiglu_half) {
         // fused SwiGLU: act[p, n] = silu(min(g, L)) * clamp(u, -L, L) from the FP32 accumulators
-        // of the gate block (b = 0) and the up block (b = 1); BF16 out, [R, swiglu_half]
+        // of the gate block (b = 0) and the up block (b = 1), each rounded to BF16 first (the
+        // pages' BF16 gate/up buffers); BF16 out, [R, swiglu_half]
         const int n0 = (ti.nb / C::NBLK) * BM + q * 32;
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t dg = D_COL + (db * C::NBLK) * C::BN_MAX;
@@ -369,7 +370,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            st[j * 32 + lane] = __float2bfloat16_rn(swiglu_clamped(__uint_as_float(g[j]), __uint_as_float(u[j]), args.limit));
+            st[j * 32 + lane] = __float2bfloat16_rn(swiglu_clamped(
+                __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[j]))),
+                __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[j]))), args.limit));
           __syncwarp();
           const int rows = min(32, ti.cnt - c0);
           for (int c = lane; c < 32 * 4; c += 32) {

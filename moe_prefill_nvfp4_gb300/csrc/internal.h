@@ -54,6 +54,8 @@ int grouped_gemm_launch(const GemmArgs& args, const void* A, int a_rows, int lda
 // I a multiple of 128), K a multiple of 256, 64-row weight maps present.
 bool pair_gemm_supported(const GemmArgs& args);
 bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half);
+// whether the automatic choice takes the pair kernel for R sorted rows over E experts
+bool pair_gemm_preferred(int R, int E);
 // token rows in expert order (the pair GEMM's contiguous A): xs[p] = x[sorted_token_ids[p]], p <
 // expert_offsets[E]
 int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,

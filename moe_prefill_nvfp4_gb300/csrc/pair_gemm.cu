@@ -19,8 +19,8 @@
 // forward copies the gate/up GEMM's gathered token rows into expert order first (one copy kernel;
 // a TMA gather4 moves only ~12 B/cycle per SM and a 256-token tile needs ~32 B/cycle, 16-byte
 // cp.async gathers from two warps measured ~8 B/cycle).  Each CTA loads the rows it holds with
-// tiled TMA boxes (16 rows x 64 k, 128-byte swizzle) whose transaction bytes complete on the even
-// CTA's barrier (the .cta_group::2 form).  There is no cluster multicast.
+// one tiled TMA box per atom (BN/2 rows x 64 k, 128-byte swizzle) whose transaction bytes complete
+// on the even CTA's barrier (the .cta_group::2 form).  There is no cluster multicast.
 //
 // Warp roles (16 warps):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global
@@ -53,8 +53,6 @@ constexpr int PAIR_ROWS = 256;
 constexpr int BKW = 256;         // k per weight stage (128 packed bytes per row)
 constexpr int BKA = 64;          // k per atom: one B stage, one TMEM A stage, four MMAs
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_WARPS = 16;
-constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int WARP_WP = 12, WARP_BP = 13, WARP_MMA = 14;
 constexpr int MAX_E = 512;
 
@@ -66,6 +64,9 @@ struct Cfg {
   static constexpr int BN = BN_;
   static constexpr int ND = ND_;
   static constexpr int NDQ = NDQ_;
+  // warps: 0-3 epilogue, 4-7 and 8-11 dequantisation, 12-14 producers and MMA, 16-19 the third
+  // dequantising warpgroup when NDQ = 3
+  static constexpr int THREADS = (NDQ == 3 ? 20 : 16) * 32;
   static constexpr int BH = BN / 2;
   static constexpr int A_COL = ND * BN;
   static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A stages = B stages
@@ -90,7 +91,7 @@ struct Cfg {
   static_assert(BN % 32 == 0 && BN <= 256 && NS >= 2, "token tile / TMEM columns");
   static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
-  static_assert(NDQ == 1 || NDQ == 2, "dequantising warpgroups");
+  static_assert(NDQ >= 1 && NDQ <= 3, "dequantising warpgroups");
 };
 
 struct Tile {
@@ -205,6 +206,34 @@ MOE_DEV void tma_load_2d_pair(uint32_t dst, const void* tmap, int x, int y, uint
       : "memory");
 }
 
+// ------------------------------------------------------------------------- dequantisation, 32 k
+
+// 32 consecutive codes of one weight row (w[j]: codes 8j..8j+7, low nibble first) with the two
+// E4M3 block scales in the low two bytes of `sc` -> 16 BF16 pairs; the arithmetic of dequant64.
+MOE_DEV void dequant32(const uint32_t (&w)[4], uint32_t sc, float s2, uint32_t (&out)[16]) {
+  uint32_t a01, a23;
+  e4m3x4_to_f16x2(sc, a01, a23);
+  const uint32_t blk[2] = {a01, a01 >> 16};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2(w[j], h);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) out[4 * j + q] = dequant_pair(h[q], blk[j >> 1], s2);
+  }
+}
+
+MOE_DEV void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+MOE_DEV float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 // ------------------------------------------------------------------------- tcgen05, pair form
 
 MOE_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -243,7 +272,7 @@ MOE_DEV void commit_pair(uint32_t bar) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,7 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // producer grid at its end)
   if (args.ready_in == nullptr) griddep_wait();
   griddep_launch_dependents();
-  for (int i = tid; i <= E; i += NUM_THREADS) s_offs[i] = args.offsets[i];
+  for (int i = tid; i <= E; i += C::THREADS) s_offs[i] = args.offsets[i];
   __syncthreads();
 
   const int NG = args.N / PAIR_ROWS;  // n-groups of 256 weight rows (gate/up: 128 act columns)
@@ -381,9 +410,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t dcol = (uint32_t)(db * C::BN);
       if (half) {
         // fused clamped SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
-        // act column a0 + (lane & 15); act = silu(min(g, L)) * clamp(u, -L, L) from the FP32
-        // accumulators (not rounded to BF16 first: against the stage-rounding reference that
-        // keeps each element within half a BF16 unit of g and u), rounded to BF16
+        // act column a0 + (lane & 15); g and u are the FP32 accumulators rounded to BF16 (the
+        // pages' BF16 gate/up buffers), act = silu(min(g, L)) * clamp(u, -L, L) rounded to BF16
         const int a0 = t.ng * 128 + (int)rank * 64 + q * 16;
         __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
         const bool is_gate = lane < 16;
@@ -402,8 +430,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // lane l < 16 keeps tokens j (its g, the partner's u); lane l + 16 tokens 16 + j
             const float mine = __uint_as_float(is_gate ? v[j] : v[16 + j]);
             const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(is_gate ? v[16 + j] : v[j]), 16);
-            const float gv = is_gate ? mine : other;
-            const float uv = is_gate ? other : mine;
+            const float gv = bf16_round(is_gate ? mine : other);
+            const float uv = bf16_round(is_gate ? other : mine);
             const int tok = is_gate ? j : 16 + j;
             st[tok * 16 + (lane & 15)] = __float2bfloat16_rn(swiglu_clamped(gv, uv, args.limit));
           }
@@ -463,12 +491,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) counter_add_release(args.ready_out + t.e, t.cnt);
       }
     }
-  } else if (warp < 4 + 4 * C::NDQ) {
+  } else if ((warp >= 4 && warp < 4 + 4 * min(C::NDQ, 2)) || warp >= 16) {
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
     // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
     // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes the atoms ai with ai % NDQ == wg.
-    const int wg = (warp - 4) >> 2;
+    const int wg = warp < 12 ? (warp - 4) >> 2 : 2;
     const int q = warp & 3;
     const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
@@ -480,11 +508,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
       const float s2 = args.scale2[t.e];
       for (int kb = 0; kb < KA; ++kb, ++ai) {
-        if (C::NDQ == 2 && (ai & 1) != wg) continue;
+        if (ai % C::NDQ != wg) continue;
         const int wi = ai >> 2;  // weight stage (4 atoms)
         const int ws = wi % NW;
         const int atom = ai & 3;
-        if (atom == (C::NDQ == 2 ? wg : 0) && !warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
+        // this warpgroup's first atom of the weight stage waits for it, its last one releases it
+        if (atom < C::NDQ && !warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
           ok = false;
           break;
         }
@@ -492,7 +521,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint4 lo = *reinterpret_cast<const uint4*>(pk + (((2 * atom) ^ (sr & 7)) << 4));
         const uint4 hi = *reinterpret_cast<const uint4*>(pk + (((2 * atom + 1) ^ (sr & 7)) << 4));
         const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16 + atom * 4);
-        if (atom == 4 - C::NDQ + wg) {  // this warp's last read of the weight stage
+        if (atom + C::NDQ > 3) {  // this warp's last read of the weight stage
           __syncwarp();
           if (lane == 0) mbar_arrive(w_empty(ws));
         }
@@ -502,10 +531,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        uint32_t out[32];
-        dequant64(w, sc, s2, out);
-        tmem_st_32x32b_x32(tmem_base + lane_addr + C::A_COL + s * 32, out);
+        // two halves of 32 k: the first half's TMEM store is in flight while the second is computed
+        const uint32_t ta = tmem_base + lane_addr + C::A_COL + s * 32;
+        {
+          const uint32_t w4[4] = {lo.x, lo.y, lo.z, lo.w};
+          uint32_t out[16];
+          dequant32(w4, sc, s2, out);
+          tmem_st_32x32b_x16(ta, out);
+        }
+        {
+          const uint32_t w4[4] = {hi.x, hi.y, hi.z, hi.w};
+          uint32_t out[16];
+          dequant32(w4, sc >> 16, s2, out);
+          tmem_st_32x32b_x16(ta + 16, out);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -545,11 +584,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == WARP_BP) {
     // ------------------------------------------------------------------ B producer
-    // Both CTAs: for each atom, this CTA's rows [p0 + rank*bn/2, p0 + (rank+1)*bn/2) of the tile,
-    // k [64 kb, 64 kb + 64), as 16-row tiled boxes whose bytes complete on the even CTA's full
-    // barrier; the even CTA's thread arrives there with the bytes of both CTAs' boxes.  Rows past
-    // the tile's count belong to the next expert (or lie past the tensor and are zero-filled): the
-    // MMA reads them into accumulator columns the epilogue never stores.
+    // Both CTAs: for each atom, one tiled box of BH rows starting at this CTA's first row p0 +
+    // rank*bn/2 of the tile, k [64 kb, 64 kb + 64), whose bytes complete on the even CTA's full
+    // barrier; the even CTA's thread arrives there with the bytes of both CTAs' boxes (one box
+    // per atom: a producer thread issues a TMA copy only every ~100-150 cycles).  The MMA reads the
+    // first bn/2 rows; rows past the tile's count belong to the next expert (or lie past the
+    // tensor and are zero-filled) and reach only accumulator columns the epilogue never stores.
     if (lane == 0) {
       int ai = 0;
       bool ok = true;
@@ -557,8 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int g = tile_at(it);
         if (g < 0) break;
         const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
-        const int nrows = t.bn >> 1;  // a multiple of 16
-        const int y0 = t.p0 + (int)rank * nrows;
+        const int y0 = t.p0 + (int)rank * (t.bn >> 1);
         if (args.ready_in != nullptr) {
           // the producer GEMM has stored every row of this expert (all its CTA tiles' epilogue warps)
           if (!wait_counter(args.ready_in + t.e, (s_offs[t.e + 1] - s_offs[t.e]) * args.ready_need * 4, s_abort,
@@ -571,10 +610,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % NS;
           if (!wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(full(s), 2u * (uint32_t)nrows * 128u);
-          const uint32_t bar = leader_addr(full(s));
-          const uint32_t dst0 = sbase + C::OFF_B + s * C::B_STAGE;
-          for (int j = 0; j < nrows; j += 16) tma_load_2d_pair(dst0 + j * 128, &bmap, kb * BKA, y0 + j, bar);
+          if (rank == 0) mbar_arrive_expect_tx(full(s), 2u * (uint32_t)C::B_STAGE);
+          tma_load_2d_pair(sbase + C::OFF_B + s * C::B_STAGE, &bmap, kb * BKA, y0, leader_addr(full(s)));
         }
       }
       if (!ok) {
@@ -632,7 +669,17 @@ using CfgWide = Cfg<256, 1, 2>;   // 256-token tiles, one accumulator
 using CfgPair = Cfg<128, 2, 2>;   // 128-token tiles, two accumulator buffers
 
 template <class C>
-int launch_cfg(const CUtensorMap& bmap, const GemmArgs& args, cudaStream_t stream) {
+int launch_cfg(const GemmArgs& args, cudaStream_t stream) {
+  CUtensorMap bmap;
+  {  // A rows (contiguous, expert order): boxes of BN/2 rows x 64 k, 128-byte swizzle
+    const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.a_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)args.lda * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BKA, (cuuint32_t)C::BH};
+    const cuuint32_t estr[2] = {1, 1};
+    const int rc = encode_tmap(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(args.A), dims, strides, box,
+                               estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != MOE_OK) return rc;
+  }
   static std::atomic<int> configured[64];
   static std::atomic<int> max_clusters[64];
   int dev = 0;
@@ -653,7 +700,7 @@ int launch_cfg(const CUtensorMap& bmap, const GemmArgs& args, cudaStream_t strea
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_ALLOC;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -680,26 +727,22 @@ bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half) {
   return N % pg::PAIR_ROWS == 0 && K % pg::BKW == 0 && E <= pg::MAX_E && (swiglu_half == 0 || swiglu_half * 2 == N);
 }
 
+// Measured on GLM widths: the pair kernel's 256-token tiles beat the single-CTA kernel once experts
+// average more than 128 rows (the 8192-row Zipf chunk: gate/up 1.81 vs 2.33 ms, down 1.14 vs
+// 1.23 ms); at ~100 rows per expert (2048 rows, 160 experts) and below the single-CTA kernel's
+// multicast activation tiles are faster (gate/up 0.74 vs 0.95 ms).
+bool pair_gemm_preferred(int R, int E) { return (double)R / E > 128.0; }
+
 bool pair_gemm_supported(const GemmArgs& args) {
   return args.wmaps64 != nullptr && args.gather == nullptr && pair_gemm_shape_ok(args.N, args.K, args.E, args.swiglu_half);
 }
 
 int pair_gemm_launch(const GemmArgs& args, cudaStream_t stream) {
   if (!pair_gemm_supported(args)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap bmap;
-  {  // A rows (contiguous, expert order): boxes of 16 rows x 64 k, 128-byte swizzle
-    const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.a_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)args.lda * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)pg::BKA, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    const int rc = encode_tmap(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(args.A), dims, strides, box,
-                               estr, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc != MOE_OK) return rc;
-  }
   // token-tile width from the mean rows per expert (the distribution itself stays on the device)
   const double mean_rows = (double)args.R / args.E;
-  if (mean_rows > 128.0) return pg::launch_cfg<pg::CfgWide>(bmap, args, stream);
-  return pg::launch_cfg<pg::CfgPair>(bmap, args, stream);
+  if (mean_rows > 128.0) return pg::launch_cfg<pg::CfgWide>(args, stream);
+  return pg::launch_cfg<pg::CfgPair>(args, stream);
 }
 
 }  // namespace moe

@@ -663,10 +663,12 @@ int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, con
 
 // ------------------------------------------------------------------------------------------------
 // token rows in expert order for the gate/up GEMM: xs[p, :] = x[sorted_token_ids[p], :] for the
-// sorted rows p < expert_offsets[E] (read on the device), 16-byte vectors, grid-stride.  A token id
-// outside [0, a_rows) records MOE_DEVERR_BAD_GATHER and copies row 0.
+// sorted rows p < expert_offsets[E] (read on the device).  A warp copies one row at a time with
+// four 16-byte loads per lane in flight before their stores (the copy is bound by the write
+// stream).  A token id outside [0, a_rows) records MOE_DEVERR_BAD_GATHER and copies row 0.
 
 constexpr int GATHER_THREADS = 256;
+constexpr int GATHER_WARPS = GATHER_THREADS / 32;
 
 __global__ void __launch_bounds__(GATHER_THREADS)
     gather_rows_kernel(const uint16_t* __restrict__ x, int a_rows, int lda, const int32_t* __restrict__ sti,
@@ -675,25 +677,32 @@ __global__ void __launch_bounds__(GATHER_THREADS)
   griddep_launch_dependents();
   const int rows = min(max(__ldg(offsets + E), 0), R);
   const int nvec = H / 8;
-  const int64_t total = (int64_t)rows * nvec;
-  for (int64_t g = (int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x; g < total;
-       g += (int64_t)gridDim.x * GATHER_THREADS) {
-    const int p = (int)(g / nvec), v = (int)(g - (int64_t)p * nvec);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int p = blockIdx.x * GATHER_WARPS + warp; p < rows; p += gridDim.x * GATHER_WARPS) {
     int tok = __ldg(sti + p);
     if ((unsigned)tok >= (unsigned)a_rows) {
-      if (v == 0) set_error(err, MOE_DEVERR_BAD_GATHER);
+      if (lane == 0) set_error(err, MOE_DEVERR_BAD_GATHER);
       tok = 0;
     }
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * lda) + v);
-    *(reinterpret_cast<uint4*>(xs + (size_t)p * H) + v) = val;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * lda);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)p * H);
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), d = __ldg(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
 int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
                        const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st) {
   const int nsm = device_sm_count();
-  const int64_t need = ((int64_t)R * (H / 8) + GATHER_THREADS - 1) / GATHER_THREADS;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)(nsm > 0 ? nsm : 148) * 8));
+  const int need = (R + GATHER_WARPS - 1) / GATHER_WARPS;
+  const int grid = std::max(1, std::min(need, (nsm > 0 ? nsm : 148) * 8));
   return launch_pdl(gather_rows_kernel, dim3(grid), dim3(GATHER_THREADS), 0, st, x, a_rows, lda, sorted_token_ids,
                     expert_offsets, E, R, H, xs, err);
 }

@@ -111,3 +111,51 @@ class DeviceBlock:
     def close(self):
         self.gu.close()
         self.dn.close()
+
+
+def bf16_stage(v64: np.ndarray) -> np.ndarray:
+    """The BF16 stage rounding of the oracle's BF16 variant (fp32, then BF16 nearest even)."""
+    from oracle import moe_oracle as O
+
+    return O._to_stage(np.asarray(v64, dtype=np.float64), "bf16")
+
+
+def bf16_bracket(v64: np.ndarray):
+    """The two BF16 values around v64: its BF16 stage rounding r, and r's neighbour on v64's other
+    side (r itself where v64 is r).  An FP32 sum of v64's terms in any order lies far closer to
+    v64 than one BF16 unit, so its BF16 rounding is one of the two."""
+    v = np.asarray(v64, dtype=np.float64)
+    r = bf16_stage(v)
+    b = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.int64)
+    away = ((v > r) & (r > 0)) | ((v < r) & (r < 0))  # step away from zero, else toward it
+    nb = np.where(away, b + 1, b - 1)
+    other = (nb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    other = np.where((v == r) | (r == 0), r, other)
+    return r, other
+
+
+def fused_act_candidates(G64: np.ndarray, I: int, limit: float):
+    """References of the fused SwiGLU epilogue, which rounds its FP32 accumulators g and u to BF16
+    before the SwiGLU: the SwiGLU over the two BF16 values around g and the two around u (the
+    oracle's rounding, and the other one an FP32 summation order may reach).  Returns [4, R, I]."""
+    from oracle import moe_oracle as O
+
+    gs = bf16_bracket(G64[:, :I])
+    us = bf16_bracket(G64[:, I:])
+    return np.stack([O.swiglu_clamp(a, b, limit) for a in gs for b in us])
+
+
+def fused_act_error(got: np.ndarray, G64: np.ndarray, I: int, limit: float):
+    """(normalised error, per-element ok) of a fused SwiGLU output against the closest of its
+    references; per element within 2^-8 of it relative (act's BF16 rounding, the FP32 SwiGLU's
+    own few ulp included) plus 1e-5 of the tensor's max."""
+    cands = fused_act_candidates(G64, I, limit)
+    d = np.abs(cands - got[None])
+    best = np.take_along_axis(cands, d.argmin(axis=0)[None], axis=0)[0]
+    bad = np.abs(got - best) > np.abs(best) * 2.0 ** -8 + 1e-5 * np.abs(best).max()
+    if bad.any():
+        idx = np.argwhere(bad)[:4]
+        for r, j in idx:
+            print("fused act element", int(r), int(j), "gpu", got[r, j], "best", best[r, j], "g", G64[r, j],
+                  "u", G64[r, I + j], "candidates", cands[:, r, j])
+    return nerr(got, best), bool(not bad.any())

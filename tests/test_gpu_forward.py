@@ -28,7 +28,7 @@ from synth import inputs as S  # noqa: E402
 
 import moe_prefill_nvfp4_gb300 as moe  # noqa: E402
 
-from gpu_helpers import TOL_BF16, TOL_EXACT, DeviceBlock, bf16_host, nerr  # noqa: E402
+from gpu_helpers import TOL_BF16, TOL_EXACT, DeviceBlock, bf16_host, fused_act_error, nerr  # noqa: E402
 
 
 @pytest.fixture(autouse=True)
@@ -82,7 +82,12 @@ def _check_full(case, separate=False):
     else:
         G = ref["G64"][:R]
         _, Y, out = _stagewise(case, dict(st, G=np.zeros((R, 2 * I))), R, wvar)
-        errs = {"act": nerr(st["act"][:R], O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))}
+        if _small_rows(case, separate):  # the small-row products apply the SwiGLU to FP32 g and u
+            errs = {"act": nerr(st["act"][:R], O.swiglu_clamp(G[:, :I], G[:, I:], case.swiglu_limit))}
+        else:  # the fused epilogue rounds g and u to BF16 first
+            e_act, ok = fused_act_error(st["act"][:R], G, I, case.swiglu_limit)
+            assert ok, "fused SwiGLU element bound"
+            errs = {"act": e_act}
     errs.update(Y=nerr(st["Y"][:R], Y), out=nerr(st["out"], out))
     if case.shared is not None:
         errs["shared"] = nerr(st["shared"], ref["shared64"])
@@ -142,8 +147,9 @@ def test_eight_row_chunk(flags):
     R = c.T * c.k
     G = ref["G64"]
     _, Y, out = _stagewise(c, dict(st, G=np.zeros((R, 2 * c.I))), R, wvar)
-    errs = dict(act=nerr(st["act"], O.swiglu_clamp(G[:, :c.I], G[:, c.I:], c.swiglu_limit)), Y=nerr(st["Y"], Y),
-                out=nerr(st["out"], out))
+    e_act = (nerr(st["act"], O.swiglu_clamp(G[:, :c.I], G[:, c.I:], c.swiglu_limit)) if flags
+             else fused_act_error(st["act"], G, c.I, c.swiglu_limit)[0])
+    errs = dict(act=e_act, Y=nerr(st["Y"], Y), out=nerr(st["out"], out))
     assert all(e < TOL_BF16 for e in errs.values()), errs
     assert nerr(st["out"], O.prefill_forward(c, "exact", logits=c.logits)["out64"]) < TOL_EXACT
 
@@ -188,13 +194,14 @@ def _check_sampled(case, tokens, variants=("bf16",)):
     rows = torch.from_numpy(t2p[tokens].reshape(-1)).long().cuda()
     Y = bf16_host(Yd[rows])
     A = bf16_host(Ad[rows])
-    # act against the SwiGLU of the oracle's unrounded G (the fused epilogue never rounds G),
+    # act against the fused epilogue's reference (the SwiGLU of the oracle's BF16-rounded G),
     # then Y and out stage by stage on the GPU's own stage inputs; weights as the GPU path uses
-    # them (BF16-rounded; FP32 for the small-row products)
+    # them (BF16-rounded; FP32 for the small-row products, whose SwiGLU takes FP32 g and u)
     dq = {}
     ref = O.token_forward(case, tokens, rid, rw, "exact" if _small_rows(case) else "bf16", dq)
     G64 = ref["G64"].reshape(-1, 2 * I)
-    ea = nerr(A, O.swiglu_clamp(G64[:, :I], G64[:, I:], case.swiglu_limit))
+    ea = (nerr(A, O.swiglu_clamp(G64[:, :I], G64[:, I:], case.swiglu_limit)) if _small_rows(case)
+          else fused_act_error(A, G64, I, case.swiglu_limit)[0])
     ys = np.stack([A[r] @ dq["dn"](int(e)).astype(np.float64).T for r, e in enumerate(rid[tokens].reshape(-1))])
     ey = nerr(Y, ys)
     perm = np.arange(len(tokens) * k, dtype=np.int32).reshape(len(tokens), k)

@@ -13,11 +13,12 @@ The oracle's per-expert stages run in worker processes (tests/oracle_pool.py, pi
 oracle's own prefill_forward).  Each check prints one ``PARITY_RECORD`` line with the measured
 normalised errors (max|gpu - ref| / max|ref|).
 
-Bounds.  Stage by stage against the BF16 variant: 4e-3 (with the SwiGLU fused into the gate/up
-epilogue there is no BF16 G stage: act is checked against the SwiGLU of the unrounded G).
-Exact-weight chain: 1e-2.  Whole BF16 chain: BF16_CHAIN_BOUND (the reading recorded with the
-design notes: the fused SwiGLU works on the FP32 accumulators, and FP32 summation order moves
-about 0.2% of G's BF16 roundings; both differences reach out through act and Y).
+Bounds.  Stage by stage against the BF16 variant: 4e-3.  Exact-weight chain: 1e-2.  Whole BF16
+chain from x: 5e-3 (BF16_CHAIN_BOUND).  out is BF16 and the oracle's out unrounded, so out's own
+rounding alone reaches up to 2^-8 = 3.9e-3 of max|out| (half a unit at the bottom of a binade);
+on top of it, FP32 summation order moves about 0.2% of G's BF16 roundings (the fused SwiGLU
+rounds its accumulators to BF16 like the oracle's G stage) and those flips reach out through act
+and Y.  Measured: 3.4e-3 to 4.2e-3.
 """
 
 import json
@@ -32,10 +33,10 @@ import moe_prefill_nvfp4_gb300 as moe  # noqa: E402
 from oracle import moe_oracle as O  # noqa: E402
 from synth import inputs as S  # noqa: E402
 
-from gpu_helpers import TOL_BF16, TOL_EXACT, DeviceBlock, bf16_host, nerr  # noqa: E402
+from gpu_helpers import TOL_BF16, TOL_EXACT, DeviceBlock, bf16_host, fused_act_error, nerr  # noqa: E402
 from oracle_pool import OraclePool, run_block, run_rows  # noqa: E402
 
-BF16_CHAIN_BOUND = 1e-2
+BF16_CHAIN_BOUND = 5e-3
 
 
 def record(name, **vals):
@@ -107,14 +108,16 @@ def test_2048_row_glm_chunk_every_element(pool, separate):
     ex = run_block(pool, c, srt, "exact", keep_g=False)
     assert not np.isnan(bf["act64"]).any() and not np.isnan(ex["Y64"]).any()
     # stage by stage on the GPU's own inputs: with the SwiGLU fused into the gate/up epilogue act is
-    # the SwiGLU of the FP32 accumulators (no BF16 G stage); separately, G and then act of the
-    # GPU's own G
+    # the SwiGLU of the BF16-rounded FP32 accumulators (no G in memory: its reference is the
+    # oracle's BF16 G, either rounding at a midpoint); separately, G and then act of the GPU's G
     G64 = bf.pop("G64")
     if separate:
         G = st["G"][:R]
         stage = {"G": nerr(G, G64), "act": nerr(act, O.swiglu_clamp(G[:, :I], G[:, I:], c.swiglu_limit))}
     else:
-        stage = {"act": nerr(act, O.swiglu_clamp(G64[:, :I], G64[:, I:], c.swiglu_limit))}
+        e_act, ok = fused_act_error(act, G64, I, c.swiglu_limit)
+        assert ok, "fused SwiGLU element bound"
+        stage = {"act": e_act}
     del G64
     stage["Y"] = nerr(Y, bf["Y64_in"])
     stage["out"] = nerr(out, O.combine_indexed(Y, st["token_to_perm"], rw))
@@ -132,7 +135,7 @@ def test_2048_row_glm_chunk_every_element(pool, separate):
 
 
 def _rows_of(db, name, rows, width):
-    t = db.ws_view(name, torch.bfloat16, (-1, width))
+    t = db.ws_view(name, torch.bfloat16, (db.case.T * db.case.k, width))
     return bf16_host(t[torch.as_tensor(np.asarray(rows), dtype=torch.long, device="cuda")])
 
 
@@ -149,8 +152,8 @@ def _sampled_check(pool, c, db, tokens, rid, rw, srt, tag):
     bf = run_rows(pool, c, srt, "bf16", rows, act_in=act, keep_g=True)
     ex = run_rows(pool, c, srt, "exact", rows)
     perm = np.arange(len(tokens) * k).reshape(len(tokens), k)
-    G64 = bf["G64"]  # the fused SwiGLU's act is the SwiGLU of the FP32 accumulators
-    e = dict(stage_act=nerr(act, O.swiglu_clamp(G64[:, :I], G64[:, I:], c.swiglu_limit)),
+    G64 = bf["G64"]  # the fused SwiGLU's act: the SwiGLU of the BF16-rounded FP32 accumulators
+    e = dict(stage_act=fused_act_error(act, G64, I, c.swiglu_limit)[0],
              stage_Y=nerr(Y, bf["Y64_in"]), bf16_chain_act=nerr(act, bf["act64"]),
              stage_out=nerr(out, O.combine_indexed(Y, perm, rw[tokens])),
              bf16_chain_out=nerr(out, O.combine_indexed(O._to_stage(bf["Y64"], "bf16"), perm, rw[tokens])),
@@ -164,8 +167,8 @@ def _sampled_check(pool, c, db, tokens, rid, rw, srt, tag):
 
 def _argmax_tokens(db, srt, R, I, H):
     sti = srt["sorted_token_ids"]
-    a = db.ws_view("act", torch.bfloat16, (-1, I))[:R]
-    y = db.ws_view("Y", torch.bfloat16, (-1, H))[:R]
+    a = db.ws_view("act", torch.bfloat16, (R, I))
+    y = db.ws_view("Y", torch.bfloat16, (R, H))
     return [int(db.out.abs().amax(1).argmax()), int(sti[int(a.abs().amax(1).argmax())]),
             int(sti[int(y.abs().amax(1).argmax())])]
 
@@ -185,7 +188,7 @@ def test_8192_row_zipf_hot_expert_rows_and_sampled_tokens(pool):
     R = int(off[-1])
     bf = run_rows(pool, c, srt, "bf16", rows, act_in=act, keep_g=True, rows_per_task=256)
     G64 = bf["G64"]
-    e_act = nerr(act, O.swiglu_clamp(G64[:, :c.I], G64[:, c.I:], c.swiglu_limit))
+    e_act = fused_act_error(act, G64, c.I, c.swiglu_limit)[0]
     e_y = nerr(Y, bf["Y64_in"])
     record("c3 hottest expert, every row", expert=hot, rows=len(rows), stage_act=e_act, stage_Y=e_y,
            bf16_chain_act=nerr(act, bf["act64"]), bf16_chain_Y=nerr(Y, bf["Y64"]))
@@ -216,10 +219,11 @@ def test_row_sweep_all_row_counts_sampled(pool):
 # ------------------------------------------------------------------------------- guard bands
 
 
+@pytest.mark.parametrize("pair", [False, True], ids=["auto-kernels", "pair-kernel"])
 @pytest.mark.parametrize("routing,T,H,I,E,k", [("router", 256, 2048, 768, 64, 8), ("biased", 300, 1024, 512, 40, 8),
                                                ("biased", 37, 512, 256, 5, 2)],
                          ids=["256-row-block", "300-rows-E40", "ragged-small"])
-def test_forward_writes_nothing_outside_its_outputs(routing, T, H, I, E, k):
+def test_forward_writes_nothing_outside_its_outputs(routing, T, H, I, E, k, pair):
     """Sentinel margins: two guard rows on each side of out, and the workspace filled with a
     pattern before the forward; afterwards the guard rows and every workspace byte past the used
     part of each buffer (up to the next buffer, and the buffers the path does not use) still hold
@@ -229,14 +233,16 @@ def test_forward_writes_nothing_outside_its_outputs(routing, T, H, I, E, k):
     big = torch.full((T + 4, H), -5.0, dtype=torch.bfloat16, device="cuda")
     db.out = big[2:T + 2]
     db.ws.fill_(0x5A)
-    db.forward()
-    torch.cuda.synchronize()
+    with moe.gemm_kernel(moe.MOE_GEMM_KERNEL_PAIR if pair else moe.MOE_GEMM_KERNEL_AUTO):
+        db.forward()
+        torch.cuda.synchronize()
     assert (big[:2] == -5.0).all() and (big[T + 2:] == -5.0).all()
     L = db.layout
     R = T * k
     used = {"logits": T * E * 4 if routing == "router" else 0, "ids": R * 4, "wts": R * 4, "sorted_token_ids": R * 4,
             "sorted_expert_ids": R * 4, "expert_offsets": (E + 1) * 4, "token_to_perm": R * 4,
-            "ready": (E + 1) * 4, "G": 0, "act": R * I * 2, "Y": R * H * 2, "x_stage": 0, "x_sorted": R * H * 2}
+            "ready": (E + 1) * 4, "G": 0, "act": R * I * 2, "Y": R * H * 2, "x_stage": 0,
+            "x_sorted": R * H * 2 if pair else 0}
     names = ["logits", "ids", "wts", "sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm",
              "sort_scratch", "ready", "G", "act", "Y", "x_stage", "x_sorted", "total"]
     ws = db.ws.cpu().numpy()

@@ -21,7 +21,7 @@ import moe_prefill_nvfp4_gb300 as moe  # noqa: E402
 from oracle import moe_oracle as O  # noqa: E402
 from synth import inputs as S  # noqa: E402
 
-from gpu_helpers import TOL_BF16, bf16_dev, bf16_host, nerr, upload  # noqa: E402
+from gpu_helpers import TOL_BF16, bf16_dev, bf16_host, fused_act_error, nerr, upload  # noqa: E402
 
 PAIR = moe.MOE_GEMM_KERNEL_PAIR
 SINGLE = moe.MOE_GEMM_KERNEL_SINGLE
@@ -135,28 +135,21 @@ def test_pair_equals_single_cta_kernel(c_dtype):
                                                   (600, 4, 2, 128, True, False), (90, 12, 4, 768, False, True)],
                          ids=["128tok", "100rows-clamped", "256tok-clamped", "identity"])
 def test_pair_swiglu_fused(T, E, k, I, big, identity):
-    """Gate/up GEMM with the clamped SwiGLU in the epilogue, act = silu(min(g, L)) * clamp(u, -L, L)
-    on the FP32 accumulators (the fused path has no BF16 G stage), against the oracle's SwiGLU of
-    its unrounded G; and within one BF16 unit of g and of u of the SwiGLU of the oracle's
-    BF16-rounded G.  `big` scales scale2 so that both clamps act."""
+    """Gate/up GEMM with the clamped SwiGLU in the epilogue (g and u rounded to BF16, then
+    act = silu(min(g, L)) * clamp(u, -L, L)) against the oracle's SwiGLU of its BF16-rounded G,
+    element by element.  `big` scales scale2 so that both clamps act."""
     c = S.make_gemm_case(T=T, E=E, k=k, N=2 * I, K=512, seed=161 + T + I, absent=(1,))
     if big:
         c.w.scale2[:] = c.w.scale2 * 200.0
     act, srt = _run(c, PAIR, identity=identity, swiglu=True, guard=1)
     G64 = _oracle(c, srt)
-    G = O.round_to_bf16(G64.astype(np.float32)).astype(np.float64)
-    ref = O.swiglu_clamp(G[:, :I], G[:, I:], 7.0)
     got = bf16_host(act)
     if big:
-        assert (np.abs(G[:, :I]) > 7.0).mean() > 0.05 and (np.abs(G[:, I:]) > 7.0).mean() > 0.05
+        assert (np.abs(G64[:, :I]) > 7.0).mean() > 0.05 and (np.abs(G64[:, I:]) > 7.0).mean() > 0.05
     o = srt["expert_offsets"]
     assert (got[o[1]:o[2]] == 0).all()
-    # per element against the SwiGLU of the unrounded G: the BF16 rounding of act (<= 2^-9
-    # relative) plus the FP32 summation-order difference of g and u carried through the SwiGLU
-    ref64 = O.swiglu_clamp(G64[:, :I], G64[:, I:], 7.0)
-    assert (np.abs(got - ref64) <= np.abs(ref64) * 2.0 ** -8 + 1e-4 * np.abs(ref64).max()).all()
-    assert nerr(got, ref64) < TOL_BF16
-    assert nerr(got, ref) < 2.0 ** -7
+    e, ok = fused_act_error(got, G64, I, 7.0)
+    assert ok and e < TOL_BF16, e
 
 
 def test_pair_refuses_gathered_rows():
@@ -175,3 +168,16 @@ def test_pair_refuses_gathered_rows():
     s = {kk: v.cpu().numpy() for kk, v in srt.items()}
     assert nerr(C.cpu().numpy().astype(np.float64), _oracle(c, s)) < 2e-6
     proj.close()
+
+
+@pytest.mark.parametrize("T,H,I,E,k,routing", [(37, 512, 256, 5, 2, "biased"), (256, 2048, 768, 64, 8, "router"),
+                                               (600, 512, 256, 4, 2, "biased")],
+                         ids=["ragged-small", "256-row-block", "300-rows-per-expert"])
+def test_forward_on_the_pair_kernel(T, H, I, E, k, routing):
+    """The whole forward with both GEMMs on CTA pairs (the gate/up token rows copied into expert
+    order first): routing and sort bit-exact, every float stage within the stage-wise bounds."""
+    from test_gpu_forward import _check_full
+
+    c = S.make_block_case(T=T, H=H, I=I, E=E, k=k, routing=routing, seed=201 + T)
+    with moe.gemm_kernel(PAIR):
+        _check_full(c)

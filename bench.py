@@ -183,7 +183,7 @@ def replica_throughput(n_ranks: int, rows_per_step: int, steps: int, max_ms: flo
     return n_ranks * rows_per_step * steps / (max_ms / 1e3)
 
 
-GEMM_SOURCES = ("grouped_gemm.cu", "common.cuh", "internal.h")
+GEMM_SOURCES = ("grouped_gemm.cu", "pair_gemm.cu", "common.cuh", "internal.h")
 
 
 def gemm_sources_digest() -> str:

@@ -395,9 +395,10 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   const bool pair = pair_gemm_supported(a) &&
                     (mode == MOE_GEMM_KERNEL_PAIR || (mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, W->E)));
   if (mode == MOE_GEMM_KERNEL_PAIR && !pair) return MOE_ERR_UNSUPPORTED_SHAPE;
-  // CTA tiles of this launch covering one output row: the producer side of the forward's GEMM
-  // overlap publishes per tile (and, for absent experts' zero rows, this many per row)
-  const int tiles = pair ? 2 * (W->N / 256) : (W->N + 255) / 256;
+  // CTA tiles of this launch covering one output row (counted once per epilogue warpgroup): the
+  // producer side of the forward's GEMM overlap publishes per tile and warp (and, for absent
+  // experts' zero rows, this many per row and warp)
+  const int tiles = pair ? 2 * (W->N / 256) * pair_gemm_epilogue_groups(a) : (W->N + 255) / 256;
   if (tiles_per_row) *tiles_per_row = tiles;
   if (ready_out != nullptr) a.ready_need = tiles;
   if (pair) return pair_gemm_launch(a, st);

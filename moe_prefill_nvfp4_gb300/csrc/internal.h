@@ -56,6 +56,9 @@ bool pair_gemm_supported(const GemmArgs& args);
 bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half);
 // whether the automatic choice takes the pair kernel for R sorted rows over E experts
 bool pair_gemm_preferred(int R, int E);
+// epilogue warpgroups of the pair kernel config the launch takes (each of their warps publishes
+// a tile's rows to the forward's GEMM overlap)
+int pair_gemm_epilogue_groups(const GemmArgs& args);
 // token rows in expert order (the pair GEMM's contiguous A): xs[p] = x[sorted_token_ids[p]], p <
 // expert_offsets[E]
 int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,

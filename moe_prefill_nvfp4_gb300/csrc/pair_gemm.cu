@@ -59,14 +59,15 @@ constexpr int MAX_E = 512;
 // BN: token-tile width (the pair's MMA N, <= 256, each CTA holds BN/2 rows of B); ND:
 // accumulator buffers (2 lets the epilogue of one tile overlap the next tile's MMAs); NDQ:
 // dequantising warpgroups.  TMEM: ND*BN accumulator columns, then NS A stages of 32 columns.
-template <int BN_, int ND_, int NDQ_>
+template <int BN_, int ND_, int NDQ_, int NEPI_ = 1>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr int ND = ND_;
   static constexpr int NDQ = NDQ_;
-  // warps: 0-3 epilogue, 4-7 and 8-11 dequantisation, 12-14 producers and MMA, 16-19 the third
-  // dequantising warpgroup when NDQ = 3
-  static constexpr int THREADS = (NDQ == 3 ? 20 : 16) * 32;
+  static constexpr int NEPI = NEPI_;  // epilogue warpgroups (2: alternate 32-column chunks)
+  // warps: 0-3 epilogue, 4-7 (and 8-11) dequantisation, 12-14 producers and MMA, 16-19 the second
+  // epilogue warpgroup when NEPI = 2
+  static constexpr int THREADS = (NEPI == 2 ? 20 : 16) * 32;
   static constexpr int BH = BN / 2;
   static constexpr int A_COL = ND * BN;
   static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A stages = B stages
@@ -79,7 +80,7 @@ struct Cfg {
   static constexpr int OFF_PK = OFF_B + NS * B_STAGE;
   static constexpr int OFF_SC = OFF_PK + NW * PK_STAGE;
   static constexpr int OFF_EPI = OFF_SC + NW * SC_STAGE;
-  static constexpr int OFF_OFFS = OFF_EPI + 4 * EPI_WARP_BYTES;
+  static constexpr int OFF_OFFS = OFF_EPI + 4 * NEPI * EPI_WARP_BYTES;
   static constexpr int OFF_TBASE = OFF_OFFS + (MAX_E + 1) * 4;
   static constexpr int OFF_BAR = (OFF_TBASE + (MAX_E + 1) * 4 + 7) & ~7;
   // barriers: full[NS] empty[NS] w_full[NW] w_empty[NW] d_full[ND] d_empty[ND] drain
@@ -91,7 +92,7 @@ struct Cfg {
   static_assert(BN % 32 == 0 && BN <= 256 && NS >= 2, "token tile / TMEM columns");
   static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
-  static_assert(NDQ >= 1 && NDQ <= 3, "dequantising warpgroups");
+  static_assert((NDQ == 1 || NDQ == 2) && (NEPI == 1 || NEPI == 2), "warpgroups");
 };
 
 struct Tile {
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int d = 0; d < ND; ++d) {
       mbar_init(d_full(d), 1);
-      mbar_init(d_empty(d), 8);  // the 4 epilogue warps of both CTAs
+      mbar_init(d_empty(d), 8 * C::NEPI);  // the epilogue warps of both CTAs
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -375,14 +376,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     return g < total ? g : -1;
   };
 
-  if (warp < 4) {
+  if (warp < 4 || warp >= 16) {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp;
-    uint8_t* stg = smem + C::OFF_EPI + q * C::EPI_WARP_BYTES;
+    // Warpgroup h of NEPI takes the 32-column chunks c0 = 32 (h + NEPI j) of each tile; a warp
+    // releases the accumulator after its last chunk's load, and publishes the tile's rows (to a
+    // consumer GEMM) after its stores, like every other epilogue warp.
+    const int q = warp & 3;
+    const int h = warp >= 16 ? 1 : 0;
+    uint8_t* stg = smem + C::OFF_EPI + (h * 4 + q) * C::EPI_WARP_BYTES;
     const bool f32 = args.c_dtype == MOE_DTYPE_F32;
     const int esz = f32 ? 4 : 2;
     const int out_cols = half ? half : args.N;
-    if (!*s_bad) {
+    if (!*s_bad && h == 0) {
       // rows of absent experts are written as zeros (the pages' zeroed routed-output rows)
       const int chunks_per_row = out_cols * esz / 16;
       for (int e = 0; e < E; ++e) {
@@ -408,6 +413,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!warp_wait_local(d_full(db), (it / ND) & 1, s_abort, args.err, limit)) break;
       tc_fence_after();
       const uint32_t dcol = (uint32_t)(db * C::BN);
+      constexpr int CSTEP = 32 * C::NEPI;
+      if (32 * h >= t.cnt) {  // no chunk for this warp in this tile
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(d_empty(db), rank);
+      }
       if (half) {
         // fused clamped SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
         // act column a0 + (lane & 15); g and u are the FP32 accumulators rounded to BF16 (the
@@ -415,11 +426,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int a0 = t.ng * 128 + (int)rank * 64 + q * 16;
         __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
         const bool is_gate = lane < 16;
-        for (int c0 = 0; c0 < t.cnt; c0 += 32) {
+        for (int c0 = 32 * h; c0 < t.cnt; c0 += CSTEP) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(lane_base + dcol + c0, v);
           tmem_wait_ld();
-          if (c0 + 32 >= t.cnt) {
+          if (c0 + CSTEP >= t.cnt) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_leader(d_empty(db), rank);
@@ -451,11 +462,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       } else {
         const int n0 = t.ng * PAIR_ROWS + (int)rank * BM + q * 32;
-        for (int c0 = 0; c0 < t.cnt; c0 += 32) {
+        for (int c0 = 32 * h; c0 < t.cnt; c0 += CSTEP) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(lane_base + dcol + c0, v);
           tmem_wait_ld();
-          if (c0 + 32 >= t.cnt) {
+          if (c0 + CSTEP >= t.cnt) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_leader(d_empty(db), rank);
@@ -491,12 +502,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0) counter_add_release(args.ready_out + t.e, t.cnt);
       }
     }
-  } else if ((warp >= 4 && warp < 4 + 4 * min(C::NDQ, 2)) || warp >= 16) {
+  } else if (warp >= 4 && warp < 4 + 4 * C::NDQ) {
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
     // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
     // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes the atoms ai with ai % NDQ == wg.
-    const int wg = warp < 12 ? (warp - 4) >> 2 : 2;
+    const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (args.ready_in != nullptr) griddep_wait();
 }
 
-using CfgWide = Cfg<256, 1, 2>;   // 256-token tiles, one accumulator
+using CfgWide = Cfg<256, 1, 2, 2>;   // 256-token tiles, one accumulator
 using CfgPair = Cfg<128, 2, 2>;   // 128-token tiles, two accumulator buffers
 
 template <class C>
@@ -733,6 +744,14 @@ bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half) {
 // multicast activation tiles are faster (gate/up 0.74 vs 0.95 ms).
 bool pair_gemm_preferred(int R, int E) { return (double)R / E > 128.0; }
 
+namespace {
+bool wide_tiles(const GemmArgs& args) { return (double)args.R / args.E > 128.0; }
+}  // namespace
+
+int pair_gemm_epilogue_groups(const GemmArgs& args) {
+  return wide_tiles(args) ? pg::CfgWide::NEPI : pg::CfgPair::NEPI;
+}
+
 bool pair_gemm_supported(const GemmArgs& args) {
   return args.wmaps64 != nullptr && args.gather == nullptr && pair_gemm_shape_ok(args.N, args.K, args.E, args.swiglu_half);
 }
@@ -740,8 +759,7 @@ bool pair_gemm_supported(const GemmArgs& args) {
 int pair_gemm_launch(const GemmArgs& args, cudaStream_t stream) {
   if (!pair_gemm_supported(args)) return MOE_ERR_UNSUPPORTED_SHAPE;
   // token-tile width from the mean rows per expert (the distribution itself stays on the device)
-  const double mean_rows = (double)args.R / args.E;
-  if (mean_rows > 128.0) return pg::launch_cfg<pg::CfgWide>(args, stream);
+  if (wide_tiles(args)) return pg::launch_cfg<pg::CfgWide>(args, stream);
   return pg::launch_cfg<pg::CfgPair>(args, stream);
 }
 

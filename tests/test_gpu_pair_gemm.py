@@ -181,3 +181,17 @@ def test_forward_on_the_pair_kernel(T, H, I, E, k, routing):
     c = S.make_block_case(T=T, H=H, I=I, E=E, k=k, routing=routing, seed=201 + T)
     with moe.gemm_kernel(PAIR):
         _check_full(c)
+
+
+@pytest.mark.parametrize("T,E", [(600, 4), (64, 6)], ids=["wide-tiles", "128-token-tiles"])
+def test_forward_pair_expert_absent_only_in_gate_up(T, E):
+    """An expert the gate/up table lacks: the gate/up launch writes its activation rows as zeros and
+    publishes them to the down launch (which otherwise waits out its bound), on both configs."""
+    from test_gpu_forward import _check_full
+
+    c = S.make_block_case(T=T, H=512, I=256, E=E, k=2, routing="biased", seed=211 + T)
+    c.gate_up.packed[1] = None
+    c.gate_up.scales[1] = None
+    with moe.gemm_kernel(PAIR):
+        _check_full(c)
+        assert moe.moe_get_device_error() == 0

@@ -530,6 +530,43 @@ class GpuBench:
         return out
 
 
+def run_gemm_only(args):
+    """Profiling driver: the two grouped GEMMs alone (gate/up with the fused SwiGLU, then down),
+    `args.gemm_only` times, on a small Zipf case at GLM widths (40 experts, 4096 rows, top-8:
+    every expert takes 256-token tiles; 0.5 GB of weights), sized for an ncu capture.  The token
+    rows are put into expert order with torch indexing (the forward does it with its own copy)."""
+    import torch
+
+    import moe_prefill_nvfp4_gb300 as moe
+    from moe_prefill_nvfp4_gb300.weights import upload_projection
+    from synth import inputs as S
+
+    torch.cuda.set_device(0)
+    case = S.make_block_case(T=4096, H=5120, I=1536, E=40, k=8, routing="zipf", seed=1003)
+    T, H, I, E, k = case.T, case.H, case.I, case.E, case.k
+    x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).cuda()
+    ids, _ = moe.moe_route_topk(torch.from_numpy(case.logits).cuda(), k)
+    srt = moe.moe_sort_by_expert(ids, E)
+    gu = upload_projection(case.gate_up.packed, case.gate_up.scales, case.gate_up.scale2, 2 * I, H, device="cuda")
+    dn = upload_projection(case.down.packed, case.down.scales, case.down.scale2, H, I, device="cuda")
+    R = T * k
+    xs = x[srt["sorted_token_ids"].long()].contiguous()
+    act = torch.empty(R, I, dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.gemm_only):
+        moe.moe_w4a16_grouped_gemm_swiglu(xs, gu.table, srt["expert_offsets"], R, limit=7.0, out=act)
+        moe.moe_w4a16_grouped_gemm(act, dn.table, srt["expert_offsets"], R, out=Y)
+    torch.cuda.synchronize()
+    err = moe.moe_get_device_error()
+    counts = np.diff(srt["expert_offsets"].cpu().numpy())
+    print(json.dumps({"gemm_only": args.gemm_only, "rows_per_expert_max": int(counts.max()),
+                      "rows_per_expert_mean": R / E, "device_error": err}), flush=True)
+    gu.close()
+    dn.close()
+    if err:
+        sys.exit(1)
+
+
 def run_gpu(args):
     import torch
 
@@ -699,10 +736,14 @@ def main():
     ap.add_argument("--sweep-rows", default=None, help="row counts of the c4 sweep (default: all eleven)")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-only", type=int, default=0,
+                    help="profiling driver: run the two grouped GEMMs this many times on a small Zipf case and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.gemm_only:
+        run_gemm_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int s = 0; s < NW; ++s) {
       mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), 4 * C::NDQ);
+      mbar_init(w_empty(s), 4);  // the 4 warps of the warpgroup that takes the stage
     }
     for (int d = 0; d < ND; ++d) {
       mbar_init(d_full(d), 1);
@@ -506,62 +506,68 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
     // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
-    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes the atoms ai with ai % NDQ == wg.
+    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes whole weight stages (256 k, four atoms)
+    // wi with wi % NDQ == wg: it reads the stage's packed bytes and scales into registers once,
+    // releases the stage, then writes the four atoms' BF16 tiles into their TMEM slots and
+    // publishes them after one wait for all eight stores.
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    int ai = 0;
+    int wi = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int g = tile_at(it);
       if (g < 0) break;
       const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
       const float s2 = args.scale2[t.e];
-      for (int kb = 0; kb < KA; ++kb, ++ai) {
-        if (ai % C::NDQ != wg) continue;
-        const int wi = ai >> 2;  // weight stage (4 atoms)
+      for (int ks = 0; ks < KW; ++ks, ++wi) {
+        if (wi % C::NDQ != wg) continue;
         const int ws = wi % NW;
-        const int atom = ai & 3;
-        // this warpgroup's first atom of the weight stage waits for it, its last one releases it
-        if (atom < C::NDQ && !warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
+        if (!warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
           ok = false;
           break;
         }
         const uint8_t* pk = smem + C::OFF_PK + ws * C::PK_STAGE + sr * 128;
-        const uint4 lo = *reinterpret_cast<const uint4*>(pk + (((2 * atom) ^ (sr & 7)) << 4));
-        const uint4 hi = *reinterpret_cast<const uint4*>(pk + (((2 * atom + 1) ^ (sr & 7)) << 4));
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16 + atom * 4);
-        if (atom + C::NDQ > 3) {  // this warp's last read of the weight stage
-          __syncwarp();
-          if (lane == 0) mbar_arrive(w_empty(ws));
+        uint4 pkv[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pkv[c] = *reinterpret_cast<const uint4*>(pk + ((c ^ (sr & 7)) << 4));
+        const uint4 scv = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(w_empty(ws));
+        const uint32_t scw[4] = {scv.x, scv.y, scv.z, scv.w};
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int ai = wi * 4 + a;
+          const int s = ai % NS;
+          if (!warp_wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ta = tmem_base + lane_addr + C::A_COL + s * 32;
+          {
+            const uint32_t w4[4] = {pkv[2 * a].x, pkv[2 * a].y, pkv[2 * a].z, pkv[2 * a].w};
+            uint32_t out[16];
+            dequant32(w4, scw[a], s2, out);
+            tmem_st_32x32b_x16(ta, out);
+          }
+          {
+            const uint32_t w4[4] = {pkv[2 * a + 1].x, pkv[2 * a + 1].y, pkv[2 * a + 1].z, pkv[2 * a + 1].w};
+            uint32_t out[16];
+            dequant32(w4, scw[a] >> 16, s2, out);
+            tmem_st_32x32b_x16(ta + 16, out);
+          }
         }
-        const int s = ai % NS;
-        if (!warp_wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // two halves of 32 k: the first half's TMEM store is in flight while the second is computed
-        const uint32_t ta = tmem_base + lane_addr + C::A_COL + s * 32;
-        {
-          const uint32_t w4[4] = {lo.x, lo.y, lo.z, lo.w};
-          uint32_t out[16];
-          dequant32(w4, sc, s2, out);
-          tmem_st_32x32b_x16(ta, out);
-        }
-        {
-          const uint32_t w4[4] = {hi.x, hi.y, hi.z, hi.w};
-          uint32_t out[16];
-          dequant32(w4, sc >> 16, s2, out);
-          tmem_st_32x32b_x16(ta + 16, out);
-        }
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_leader(full(s), rank);
+        if (lane == 0)
+          for (int a = 0; a < 4; ++a) arrive_leader(full((wi * 4 + a) % NS), rank);
       }
     }
+    if (!ok) tmem_wait_st();  // no TMEM store of this warp outlives it
   } else if (warp == WARP_WP) {
     // ------------------------------------------------------------------ weight producer
     if (lane == 0) {

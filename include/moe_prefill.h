@@ -270,15 +270,15 @@ int moe_w4a16_grouped_gemv_swiglu(const uint16_t* A, int a_rows, int lda, const 
  *   gate = x W_gate^T, up = x W_up^T (BF16 out), act = silu(min(gate, L)) * clamp(up, -L, L)
  *   (BF16), shared_out = act W_down^T (BF16),
  * FP32 accumulation.  Its output joins the routed sum in moe_prefill_forward's combine.
- * The three products are plain dense GEMMs and run in cuBLAS; the SwiGLU is this library's.
+ * Three launches of this library's kernels: one dense tensor-core GEMM for gate and up (written
+ * as gate | up into the workspace), the SwiGLU, and one dense tensor-core GEMM for down.
  *   x          device BF16 [T, H]
  *   w_gate, w_up device BF16 [I, H];  w_down device BF16 [H, I]
  *   ws, ws_bytes device workspace of at least moe_shared_expert_workspace_bytes(T, H, I) bytes,
- *              256-byte aligned (it includes the cuBLAS workspace: nothing is allocated per call)
+ *              256-byte aligned: gate | up [T, 2I] BF16 at offset 0, then act [T, I] BF16 at the
+ *              next multiple of 256 bytes (nothing is allocated per call)
  *   shared_out device BF16 [T, H] (output)
  * Requirements: T >= 1, H and I multiples of 8, buffers 16-byte aligned, 0 < limit.
- * The first call on a device creates its cuBLAS handle: make it before any stream capture that
- * includes this call.  Calls from several host threads are serialised on the host.
  */
 size_t moe_shared_expert_workspace_bytes(int T, int H, int I);
 int moe_shared_expert_forward(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,

@@ -2,8 +2,8 @@
 
 Each ``csrc/*.cu`` file is compiled in parallel (``-gencode arch=compute_103a,code=sm_103a``),
 then linked into one shared library against the shared CUDA runtime (the same libcudart that
-PyTorch loads, so streams and the primary context are shared) and cuBLAS (the shared expert's
-plain dense GEMMs).  No cmake, no torch extension machinery: the library exports a plain C ABI
+PyTorch loads, so streams and the primary context are shared) and nothing else: every product,
+the shared expert's dense ones included, runs in this library's own kernels.  No cmake, no torch extension machinery: the library exports a plain C ABI
 (``include/moe_prefill.h``).
 """
 
@@ -79,7 +79,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                 print(log, file=sys.stderr)
     tmp = lib_path() + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp] + [o for o, _ in results] + [
-        "-lcublas", "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+        "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -505,8 +505,8 @@ int moe_combine_indexed(const uint16_t* Y, const int32_t* token_to_perm, const f
 
 size_t moe_shared_expert_workspace_bytes(int T, int H, int I) {
   if (T < 1 || H < 8 || H % 8 != 0 || I < 8 || I % 8 != 0) return 0;
-  size_t a, b, c;
-  return shared_expert_ws_layout(T, I, &a, &b, &c);
+  size_t a, b;
+  return shared_expert_ws_layout(T, I, &a, &b);
 }
 
 int moe_shared_expert_forward(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,

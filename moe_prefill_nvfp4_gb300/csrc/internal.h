@@ -123,10 +123,26 @@ struct SmallRowsArgs {
 };
 int small_rows_launch(const SmallRowsArgs& a, cudaStream_t st);
 
-// shared expert (shared_expert.cu): workspace = gate|up [T, 2I] BF16, act [T, I] BF16 and the
-// cuBLAS workspace, each 256-byte aligned; returns the total bytes
-constexpr size_t kSharedExpertBlasWorkspace = size_t(32) << 20;
-size_t shared_expert_ws_layout(int T, int I, size_t* off_gu, size_t* off_act, size_t* off_blas);
+// Dense BF16 GEMM on the tensor cores (dense_gemm.cu): for each weight segment s < nseg,
+// C[t, col[s] + n] = sum_k B[t, k] W[s][n, k] (t < T, n < rows[s], k < K), FP32 accumulation, BF16
+// out.  B [T, K] with row stride ldb, W[s] [rows[s], K] with row stride ldw[s], C row stride ldc
+// (elements); K, strides, rows and col multiples of 8, pointers 16-byte aligned.
+struct DenseGemm {
+  const uint16_t* B;
+  int T, K, ldb;
+  int nseg;
+  const uint16_t* W[2];
+  int rows[2], ldw[2], col[2];
+  uint16_t* C;
+  int ldc;
+};
+int dense_gemm_launch(const DenseGemm& d, cudaStream_t stream);
+// token-tile width the launch takes for T tokens over weight_tiles tiles of 128 weight rows
+int dense_gemm_token_tile(int T, int weight_tiles, int nsm);
+
+// shared expert (shared_expert.cu): workspace = gate|up [T, 2I] BF16 and act [T, I] BF16, each
+// 256-byte aligned; returns the total bytes
+size_t shared_expert_ws_layout(int T, int I, size_t* off_gu, size_t* off_act);
 int shared_expert_launch(const uint16_t* x, int T, int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
                          const uint16_t* w_down, float limit, void* ws, uint16_t* shared_out, cudaStream_t st);
 

@@ -129,7 +129,8 @@ def test_forward_rejects(L):
 def test_shared_expert_rejects_and_sizes(L):
     T, H, I = 4, 2048, 768
     need = L.moe_shared_expert_workspace_bytes(T, H, I)
-    assert need >= (32 << 20) + T * 3 * I * 2  # gate|up, act and the cuBLAS workspace
+    assert need >= T * 3 * I * 2  # gate|up and act
+    assert need < (1 << 20)  # nothing but the two stage buffers
     assert L.moe_shared_expert_workspace_bytes(T, H, 12) == 0  # I % 8
     f = L.moe_shared_expert_forward
     W = ctypes.c_void_p(256)

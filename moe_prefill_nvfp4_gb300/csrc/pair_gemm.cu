@@ -96,13 +96,13 @@ struct Cfg {
 };
 
 struct Tile {
-  int e, ng, p0, cnt, bn;
+  int e, ng, p0, cnt;
 };
 
 // Tile g -> (expert, n-group of 256 weight rows, token rows).  Expert e owns tiles
 // [tbase[e], tbase[e+1]): ntt token tiles x NG n-groups, n-group fastest, so the pairs running at
-// the same time share token rows (and the expert's weights) in L2.  bn: the token count rounded up
-// to 32 (each CTA then loads whole 16-row boxes).
+// the same time share token rows (and the expert's weights) in L2.  An expert's token rows are
+// split into equal chunks (multiples of 32) over its ntt token tiles.
 template <int BN>
 MOE_DEV Tile decode(int g, const int* tbase, const int* offs, int E, int NG) {
   int lo = 0, hi = E - 1;
@@ -120,7 +120,6 @@ MOE_DEV Tile decode(int g, const int* tbase, const int* offs, int E, int NG) {
   const int chunk = (((m + ntt - 1) / ntt) + 31) & ~31;
   t.p0 = offs[lo] + tt * chunk;
   t.cnt = min(chunk, m - tt * chunk);
-  t.bn = (t.cnt + 31) & ~31;
   return t;
 }
 
@@ -152,6 +151,20 @@ MOE_DEV bool wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_fla
       return false;
     }
   }
+}
+
+MOE_DEV bool warp_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
+  bool ok = true;
+  if (lane_id() == 0) ok = wait_cluster(bar, parity, abort_flag, err, limit);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// true in one lane of the (converged) warp
+MOE_DEV bool elect_one() {
+  uint32_t pred;
+  asm volatile("{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.b32 %0, 1, 0, p;\n}"
+               : "=r"(pred));
+  return pred != 0;
 }
 
 MOE_DEV bool warp_wait_local(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
@@ -602,11 +615,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   } else if (warp == WARP_BP) {
     // ------------------------------------------------------------------ B producer
     // Both CTAs: for each atom, one tiled box of BH rows starting at this CTA's first row p0 +
-    // rank*bn/2 of the tile, k [64 kb, 64 kb + 64), whose bytes complete on the even CTA's full
+    // rank*BH of the tile, k [64 kb, 64 kb + 64), whose bytes complete on the even CTA's full
     // barrier; the even CTA's thread arrives there with the bytes of both CTAs' boxes (one box
-    // per atom: a producer thread issues a TMA copy only every ~100-150 cycles).  The MMA reads the
-    // first bn/2 rows; rows past the tile's count belong to the next expert (or lie past the
-    // tensor and are zero-filled) and reach only accumulator columns the epilogue never stores.
+    // per atom: a producer thread issues a TMA copy only every ~100-150 cycles).  The MMA always
+    // has N = BN (accumulator column j = token row p0 + j): rows past the tile's count belong to
+    // the next expert (or lie past the tensor and are zero-filled) and reach only accumulator
+    // columns the epilogue never stores.  Narrower MMAs for short tiles measured slower.
     if (lane == 0) {
       int ai = 0;
       bool ok = true;
@@ -614,7 +628,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int g = tile_at(it);
         if (g < 0) break;
         const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
-        const int y0 = t.p0 + (int)rank * (t.bn >> 1);
+        const int y0 = t.p0 + (int)rank * C::BH;
         if (args.ready_in != nullptr) {
           // the producer GEMM has stored every row of this expert (all its CTA tiles' epilogue warps)
           if (!wait_counter(args.ready_in + t.e, (s_offs[t.e + 1] - s_offs[t.e]) * args.ready_need * 4, s_abort,
@@ -641,32 +655,42 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    // The whole warp walks the schedule (its descriptors and addresses stay warp-uniform); one
+    // elected lane issues each MMA and commit.
+    if (rank == 0) {
       int ai = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int g = tile_at(it);
         if (g < 0) break;
-        const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
         const int db = it % ND;
-        if (!wait_cluster(d_empty(db), ((it / ND) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
+        if (!warp_wait_cluster(d_empty(db), ((it / ND) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t idesc = make_idesc_bf16(PAIR_ROWS, t.bn);
+        const uint32_t idesc = make_idesc_bf16(PAIR_ROWS, C::BN);
         const uint64_t bdesc0 = make_sdesc_sw128(sbase + C::OFF_B);
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * C::BN);
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % NS;
-          if (!wait_cluster(full(s), (ai / NS) & 1, s_abort, args.err, limit)) { ok = false; break; }
+          if (!warp_wait_cluster(full(s), (ai / NS) & 1, s_abort, args.err, limit)) { ok = false; break; }
           tc_fence_after();
           const uint64_t bdesc = bdesc0 + (uint64_t)((s * C::B_STAGE) >> 4);
-          mma4_pair(d_tmem, tmem_base + C::A_COL + s * 32, bdesc, idesc, kb != 0);
-          commit_pair(empty(s));
+          if (elect_one()) {
+            mma4_pair(d_tmem, tmem_base + C::A_COL + s * 32, bdesc, idesc, kb != 0);
+            commit_pair(empty(s));
+          }
+          __syncwarp();
         }
-        if (ok) commit_pair(d_full(db));
+        if (ok) {
+          if (elect_one()) commit_pair(d_full(db));
+          __syncwarp();
+        }
       }
       if (!ok) {  // let every issued MMA finish before TMEM is freed
-        commit_pair(drain_bar);
-        mbar_wait_drain(drain_bar, 0);
+        if (elect_one()) {
+          commit_pair(drain_bar);
+          mbar_wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
       }
     }
   }

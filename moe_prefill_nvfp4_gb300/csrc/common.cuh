@@ -31,6 +31,16 @@ MOE_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_g
 
 MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// true in exactly one lane of the converged warp.  An issuing role (MMA, TMA) that walks its
+// schedule with the whole warp and issues from the elected lane keeps its descriptors and
+// addresses warp-uniform (measured faster in the CTA-pair GEMM than the loop run by lane 0 alone).
+MOE_DEV bool elect_one() {
+  uint32_t pred;
+  asm volatile("{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.b32 %0, 1, 0, p;\n}"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------------------------------------
 // mbarrier
 

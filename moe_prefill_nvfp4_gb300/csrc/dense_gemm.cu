@@ -181,13 +181,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp walks the schedule (warp-uniform descriptors), one elected lane issues
+    {
       const uint32_t idesc = make_idesc_bf16(BM, C::BN);
       int i = 0, it = 0;
       bool ok = true;
       for (int g = blockIdx.x; ok && g < args.total; g += tiles_t, ++it) {
         const int db = it & 1;
-        if (!wait_bounded(d_empty(db), ((it >> 1) & 1) ^ 1, s_abort, args.err, limit)) {
+        if (!warp_wait_bounded(d_empty(db), ((it >> 1) & 1) ^ 1, s_abort, args.err, limit)) {
           ok = false;
           break;
         }
@@ -195,20 +196,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * C::BN);
         for (int kb = 0; kb < KA; ++kb, ++i) {
           const int s = i % NS;
-          if (!wait_bounded(full(s), (i / NS) & 1, s_abort, args.err, limit)) {
+          if (!warp_wait_bounded(full(s), (i / NS) & 1, s_abort, args.err, limit)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t st = sbase + s * C::STAGE;
-          mma4_bf16_ss(d_tmem, make_sdesc_sw128(st), make_sdesc_sw128(st + A_STAGE), idesc, kb != 0);
-          mma_commit(empty(s));
+          if (elect_one()) {
+            mma4_bf16_ss(d_tmem, make_sdesc_sw128(st), make_sdesc_sw128(st + A_STAGE), idesc, kb != 0);
+            mma_commit(empty(s));
+          }
+          __syncwarp();
         }
-        if (ok) mma_commit(d_full(db));
+        if (ok) {
+          if (elect_one()) mma_commit(d_full(db));
+          __syncwarp();
+        }
       }
       if (!ok) {  // every issued MMA completes before TMEM is freed
-        mma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0);
+        if (elect_one()) {
+          mma_commit(drain_bar);
+          mbar_wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
       }
     }
   } else {

@@ -159,14 +159,6 @@ MOE_DEV bool warp_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abor
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// true in one lane of the (converged) warp
-MOE_DEV bool elect_one() {
-  uint32_t pred;
-  asm volatile("{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.b32 %0, 1, 0, p;\n}"
-               : "=r"(pred));
-  return pred != 0;
-}
-
 MOE_DEV bool warp_wait_local(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit) {
   bool ok = true;
   if (lane_id() == 0) ok = wait_local(bar, parity, abort_flag, err, limit);

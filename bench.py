@@ -584,6 +584,11 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     gb = GpuBench(args, dev)
+    if args.sweep_only:  # profiling driver: the c4 forward at the given row counts, nothing else
+        rows = S.SWEEP_ROWS if args.sweep_rows is None else tuple(int(v) for v in args.sweep_rows.split(","))
+        print(json.dumps({"c4_sweep": {"workload": C4_DESC, "points": gb.sweep(rows, args.steps, args.warmup)}}),
+              flush=True)
+        return
     clocks = ClockSampler(local)
     head = gb.block(args.workload, S.workload(args.workload), args.steps, args.warmup, clocks=clocks)
     cpu = None
@@ -737,6 +742,8 @@ def main():
     ap.add_argument("--reports", default="c1,c2,c0,c4",
                     help="extra workloads in the same line: any of c0,c1,c2,c1s,c4 (comma-separated) or none")
     ap.add_argument("--sweep-rows", default=None, help="row counts of the c4 sweep (default: all eleven)")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="profiling driver: run only the c4 sweep (at --sweep-rows) and print its points")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-only", type=int, default=0,

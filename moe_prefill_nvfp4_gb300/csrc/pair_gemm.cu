@@ -240,6 +240,27 @@ MOE_DEV void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
 
 MOE_DEV float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
+// 16 TMEM lanes x 32 columns: register 4i + k of thread t holds lane (t / 4) + 8 (k / 2), column
+// 8i + 2 (t % 4) + (k % 2) relative to taddr (the layout of an m16n8 MMA accumulator fragment).
+MOE_DEV void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Four 8x8 BF16 matrices, each held as one register per thread in the m16n8 fragment layout
+// (thread t: row t / 4, columns 2 (t % 4) and + 1), stored transposed: row j of matrix m goes to
+// the 16 bytes at the address thread 8m + j supplies (column j of the fragment).
+MOE_DEV void stmatrix_x4_trans(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
 // ------------------------------------------------------------------------- tcgen05, pair form
 
 MOE_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -389,6 +410,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int q = warp & 3;
     const int h = warp >= 16 ? 1 : 0;
     uint8_t* stg = smem + C::OFF_EPI + (h * 4 + q) * C::EPI_WARP_BYTES;
+    const uint32_t stg_u32 = smem_u32(stg);
     const bool f32 = args.c_dtype == MOE_DTYPE_F32;
     const int esz = f32 ? 4 : 2;
     const int out_cols = half ? half : args.N;
@@ -425,15 +447,69 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0) arrive_leader(d_empty(db), rank);
       }
       if (half) {
-        // fused clamped SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
-        // act column a0 + (lane & 15); g and u are the FP32 accumulators rounded to BF16 (the
-        // pages' BF16 gate/up buffers), act = silu(min(g, L)) * clamp(u, -L, L) rounded to BF16
+        // fused clamped SwiGLU.  TMEM lanes 32q..32q+15 hold 16 gate rows, 32q+16..32q+31 the
+        // matching up rows (act columns a0..a0+15): two 16x256b loads give each thread the gate
+        // and the up accumulator of the same (act column, token) pairs.  g and u are rounded to
+        // BF16 (the pages' BF16 gate/up buffers), act = silu(min(g, L)) * clamp(u, -L, L) rounded
+        // to BF16; transposing matrix stores stage [token][16 act columns] for 16-byte rows out.
         const int a0 = t.ng * 128 + (int)rank * 64 + q * 16;
-        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
-        const bool is_gate = lane < 16;
         for (int c0 = 32 * h; c0 < t.cnt; c0 += CSTEP) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(lane_base + dcol + c0, v);
+          uint32_t vg[16], vu[16];
+          tmem_ld_16x256b_x4(lane_base + dcol + c0, vg);
+          tmem_ld_16x256b_x4(lane_base + (16u << 16) + dcol + c0, vu);
+          tmem_wait_ld();
+          if (c0 + CSTEP >= t.cnt) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_leader(d_empty(db), rank);
+          }
+          // register 4i + k: act column (lane / 4) + 8 (k / 2), token 8i + 2 (lane % 4) + (k % 2)
+          uint32_t pk[4][2];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float a[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              a[k] = swiglu_clamped(bf16_round(__uint_as_float(vg[4 * i + k])),
+                                    bf16_round(__uint_as_float(vu[4 * i + k])), args.limit);
+            pk[i][0] = pack_bf16x2(a[0], a[1]);
+            pk[i][1] = pack_bf16x2(a[2], a[3]);
+          }
+          __syncwarp();
+          // matrix m of instruction k2: token block 2 k2 + (m >> 1), act columns 8 (m & 1) + 0..7;
+          // this lane addresses row (lane & 7) of matrix lane >> 3; the 16-byte half of a 32-byte
+          // staged row is swizzled by bit 2 of the token (conflict-free stores)
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int m = lane >> 3;
+            const int j = 8 * (2 * k2 + (m >> 1)) + (lane & 7);
+            const uint32_t addr = stg_u32 + j * 32 + (((m & 1) ^ ((j >> 2) & 1)) << 4);
+            stmatrix_x4_trans(addr, pk[2 * k2][0], pk[2 * k2][1], pk[2 * k2 + 1][0], pk[2 * k2 + 1][1]);
+          }
+          __syncwarp();
+          const int rows = min(32, t.cnt - c0);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int c = lane + 32 * r;
+            const int j = c >> 1, p = c & 1;
+            if (j < rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 32 + ((p ^ ((j >> 2) & 1)) << 4));
+              uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + (size_t)(t.p0 + c0 + j) * args.ldc + a0 + p * 8;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+          __syncwarp();
+        }
+      } else if (!f32) {
+        // BF16 output: two 16x256b loads (TMEM lanes 32q + 0..15 and + 16..31) give each thread
+        // pairs of adjacent tokens of one weight row; transposing matrix stores stage [token][32
+        // outputs] (64-byte rows, 16-byte chunks swizzled by bits 1-2 of the token) for 16-byte
+        // rows out
+        const int n0 = t.ng * PAIR_ROWS + (int)rank * BM + q * 32;
+        for (int c0 = 32 * h; c0 < t.cnt; c0 += CSTEP) {
+          uint32_t va[16], vb[16];
+          tmem_ld_16x256b_x4(lane_base + dcol + c0, va);
+          tmem_ld_16x256b_x4(lane_base + (16u << 16) + dcol + c0, vb);
           tmem_wait_ld();
           if (c0 + CSTEP >= t.cnt) {
             tc_fence_before();
@@ -441,31 +517,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (lane == 0) arrive_leader(d_empty(db), rank);
           }
           __syncwarp();
+          // instruction i: token block i; matrix m: output columns 8m..8m+7 (va: m < 2, vb: m >= 2)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            // lane l < 16 keeps tokens j (its g, the partner's u); lane l + 16 tokens 16 + j
-            const float mine = __uint_as_float(is_gate ? v[j] : v[16 + j]);
-            const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(is_gate ? v[16 + j] : v[j]), 16);
-            const float gv = bf16_round(is_gate ? mine : other);
-            const float uv = bf16_round(is_gate ? other : mine);
-            const int tok = is_gate ? j : 16 + j;
-            st[tok * 16 + (lane & 15)] = __float2bfloat16_rn(swiglu_clamped(gv, uv, args.limit));
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t p0 = pack_bf16x2(__uint_as_float(va[4 * i]), __uint_as_float(va[4 * i + 1]));
+            const uint32_t p1 = pack_bf16x2(__uint_as_float(va[4 * i + 2]), __uint_as_float(va[4 * i + 3]));
+            const uint32_t p2 = pack_bf16x2(__uint_as_float(vb[4 * i]), __uint_as_float(vb[4 * i + 1]));
+            const uint32_t p3 = pack_bf16x2(__uint_as_float(vb[4 * i + 2]), __uint_as_float(vb[4 * i + 3]));
+            const int m = lane >> 3;
+            const int j = 8 * i + (lane & 7);
+            stmatrix_x4_trans(stg_u32 + j * 64 + ((m ^ ((j >> 1) & 3)) << 4), p0, p1, p2, p3);
           }
           __syncwarp();
           const int rows = min(32, t.cnt - c0);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int c = lane + 32 * i;
-            const int r = c >> 1, h = c & 1;
-            if (r < rows) {
-              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 + h * 16);
-              uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + (size_t)(t.p0 + c0 + r) * args.ldc + a0 + h * 8;
+          for (int r = 0; r < 4; ++r) {
+            const int c = lane + 32 * r;
+            const int j = c >> 2, p = c & 3;
+            if (j < rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 64 + ((p ^ ((j >> 1) & 3)) << 4));
+              uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + (size_t)(t.p0 + c0 + j) * args.ldc + n0 + p * 8;
               *reinterpret_cast<uint4*>(dst) = val;
             }
           }
           __syncwarp();
         }
       } else {
+        // FP32 output (tests and standalone calls): stage [token][32 outputs] through registers
         const int n0 = t.ng * PAIR_ROWS + (int)rank * BM + q * 32;
         for (int c0 = 32 * h; c0 < t.cnt; c0 += CSTEP) {
           uint32_t v[32];
@@ -477,24 +555,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (lane == 0) arrive_leader(d_empty(db), rank);
           }
           __syncwarp();
-          if (f32) {
-            float* s = reinterpret_cast<float*>(stg);
+          float* sf = reinterpret_cast<float*>(stg);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __uint_as_float(v[j]);
-          } else {
-            __nv_bfloat16* s = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          }
+          for (int j = 0; j < 32; ++j) sf[j * 32 + lane] = __uint_as_float(v[j]);
           __syncwarp();
           const int rows = min(32, t.cnt - c0);
-          const int cpr = 32 * esz / 16;  // 16-byte chunks per staged row (4 bf16, 8 f32)
-          for (int c = lane; c < 32 * cpr; c += 32) {
-            const int r = c / cpr, cc = c - r * cpr;
+          for (int c = lane; c < 32 * 8; c += 32) {
+            const int r = c >> 3, cc = c & 7;
             if (r < rows) {
-              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 * esz + cc * 16);
-              uint8_t* dst = reinterpret_cast<uint8_t*>(args.C) +
-                             ((size_t)(t.p0 + c0 + r) * args.ldc + n0 + cc * (16 / esz)) * esz;
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 128 + cc * 16);
+              float* dst = reinterpret_cast<float*>(args.C) + (size_t)(t.p0 + c0 + r) * args.ldc + n0 + cc * 4;
               *reinterpret_cast<uint4*>(dst) = val;
             }
           }

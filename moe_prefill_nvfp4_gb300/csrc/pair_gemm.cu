@@ -93,6 +93,12 @@ struct Cfg {
   static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
   static_assert((NDQ == 1 || NDQ == 2) && (NEPI == 1 || NEPI == 2), "warpgroups");
+  // A dequantising warpgroup takes whole weight stages (four atoms) and waits on the four atoms'
+  // slots by phase parity; with NS >= 4 NDQ each slot has one writing warpgroup, whose successive
+  // uses of it are a completed phase apart.  Fewer slots let a warpgroup's parity wait pass on the
+  // phase before the one it needs (the other warpgroup's use still pending), which breaks the
+  // barriers' arrival and transaction counts.
+  static_assert(NS >= 4 * NDQ && NS % (4 * NDQ) == 0, "A stages per dequantising warpgroup");
 };
 
 struct Tile {

@@ -33,8 +33,8 @@ def _restore():
     moe.moe_get_device_error()
 
 
-def _case():
-    c = S.make_gemm_case(T=96, E=6, k=2, N=256, K=512, seed=181)
+def _case(T=96, E=6):
+    c = S.make_gemm_case(T=T, E=E, k=2, N=256, K=512, seed=181)
     srt = moe.moe_sort_by_expert(torch.from_numpy(c.ids).cuda(), c.E)
     return c, srt, upload(c.w)
 
@@ -44,8 +44,11 @@ def _oracle(c, s):
     return O.grouped_gemm(O.bf16_bits_to_f64(c.x), s["expert_offsets"], wfn, s["sorted_token_ids"])
 
 
-def test_wait_runs_out_and_the_kernel_returns():
-    c, srt, proj = _case()
+@pytest.mark.parametrize("T,E", [(96, 6), (600, 4)], ids=["128-token-tiles", "256-token-tiles"])
+def test_wait_runs_out_and_the_kernel_returns(T, E):
+    """Both CTA-pair configurations: dequantised weights in tensor memory (16 rows per expert) and
+    in shared memory (300 rows per expert)."""
+    c, srt, proj = _case(T, E)
     R = c.T * c.k
     x = bf16_dev(c.x)
     never = torch.zeros(c.E, dtype=torch.int32, device="cuda")  # nothing ever publishes

@@ -294,7 +294,7 @@ typedef struct {
   float swiglu_limit;     /* L, e.g. 7.0 */
   int renormalize;        /* 1: renormalise the top-k weights */
   float routed_scale;     /* multiplier of the routing weights, e.g. 1.0 */
-  int flags;              /* 0, or MOE_FWD_SEPARATE_SWIGLU */
+  int flags;              /* 0, or MOE_FWD_SEPARATE_SWIGLU | MOE_FWD_SMALL_ROWS | MOE_FWD_NO_MULTICAST */
 } moe_prefill_config;
 
 /* moe_prefill_config.flags: run the SwiGLU as its own kernel on a materialised G [R, 2I]
@@ -304,6 +304,11 @@ typedef struct {
  * (moe_w4a16_grouped_gemv*: FP32 dequantised weights, the numerics of the pages' decode GEMV)
  * instead of the tensor-core GEMMs (faster on this GPU: see the small-row products' header). */
 #define MOE_FWD_SMALL_ROWS 2
+/* moe_prefill_config.flags: no cluster-multicast TMA loads (the single-CTA GEMM's activation
+ * tiles are then loaded by each CTA itself).  For runs on more than one GPU (expert parallelism,
+ * "Module forward_prefill_gemm", "Layout compatibility": remote experts as NULL table entries,
+ * the caller all-reducing out), where this library keeps multicast out; results are identical. */
+#define MOE_FWD_NO_MULTICAST 4
 
 /* Workspace bytes for moe_prefill_forward with up to max_rows rows (0 on a bad config). */
 size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);

@@ -23,7 +23,7 @@ __all__ = [
     "moe_router_logits", "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
     "moe_sort_by_expert_noalloc", "MOE_SORT_NOALLOC_MAX_INTS",
     "moe_w4a16_grouped_gemm", "moe_w4a16_grouped_gemm_swiglu", "MOE_FWD_SEPARATE_SWIGLU", "moe_dequant_nvfp4",
-    "moe_w4a16_grouped_gemv", "moe_w4a16_grouped_gemv_swiglu", "MOE_FWD_SMALL_ROWS", "moe_swiglu_clamp", "moe_combine_indexed",
+    "moe_w4a16_grouped_gemv", "moe_w4a16_grouped_gemv_swiglu", "MOE_FWD_SMALL_ROWS", "MOE_FWD_NO_MULTICAST", "moe_swiglu_clamp", "moe_combine_indexed",
     "moe_workspace_bytes", "moe_workspace_layout", "moe_prefill_forward", "moe_get_device_error",
     "moe_shared_expert_workspace_bytes", "moe_shared_expert_forward",
     "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FWD_NUM_EVENTS", "DEVERR",
@@ -39,6 +39,7 @@ MOE_DTYPE_F32 = 1
 MOE_FWD_NUM_EVENTS = 8
 MOE_FWD_SEPARATE_SWIGLU = 1  # moe_prefill_config.flags: SwiGLU as its own kernel on a materialised G
 MOE_FWD_SMALL_ROWS = 2  # moe_prefill_config.flags: small-row products (FP32 weights) for chunks of <= 8 rows
+MOE_FWD_NO_MULTICAST = 4  # moe_prefill_config.flags: no cluster-multicast loads (runs on more than one GPU)
 MOE_SORT_NOALLOC_MAX_INTS = 65536  # int32 entries of the library's fixed sort scratch
 MOE_GEMM_KERNEL_AUTO = 0  # moe_debug_set_gemm_kernel: CTA-pair kernel where its shapes allow
 MOE_GEMM_KERNEL_SINGLE = 1  # the single-CTA kernel

@@ -354,7 +354,7 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
                         const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st,
                         int swiglu_half = 0, float limit = 0.f, int* ready_out = nullptr,
                         const int* ready_in = nullptr, int ready_need = 0, int* tile_counter = nullptr,
-                        int* tiles_per_row = nullptr) {
+                        int* tiles_per_row = nullptr, bool no_multicast = false) {
   if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
   if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (swiglu_half && (c_dtype != MOE_DTYPE_BF16 || W->N != 2 * swiglu_half || swiglu_half % 128 != 0))
@@ -391,6 +391,7 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.A = A;
   a.lda = lda;
   a.wait_ns = gemm_wait_limit_ns();
+  a.max_cluster = no_multicast ? 1 : 8;
   const int mode = g_gemm_kernel.load(std::memory_order_relaxed);
   const bool pair = pair_gemm_supported(a) &&
                     (mode == MOE_GEMM_KERNEL_PAIR || (mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, W->E)));
@@ -529,7 +530,7 @@ static bool cfg_ok(const moe_prefill_config* c) {
   return c != nullptr && c->hidden >= 256 && c->hidden % 256 == 0 && c->moe_intermediate >= 256 &&
          c->moe_intermediate % 256 == 0 && c->num_experts >= 1 && c->num_experts <= 512 && c->top_k >= 1 &&
          c->top_k <= 32 && c->top_k <= c->num_experts &&
-         (c->flags & ~(MOE_FWD_SEPARATE_SWIGLU | MOE_FWD_SMALL_ROWS)) == 0;
+         (c->flags & ~(MOE_FWD_SEPARATE_SWIGLU | MOE_FWD_SMALL_ROWS | MOE_FWD_NO_MULTICAST)) == 0;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -650,6 +651,7 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   // so the SMs the gate/up launch leaves early take more of the down work.  The sort clears them.
   const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   const bool overlap = !small && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
+  const bool no_mc = (cfg->flags & MOE_FWD_NO_MULTICAST) != 0;
   int32_t* ready = overlap ? reinterpret_cast<int32_t*>(base + L.ready) : nullptr;
   int producer_tiles = 0;
   if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, E + 1)) != MOE_OK) return rc;
@@ -667,28 +669,30 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     if (rc != MOE_OK) return rc;
     ev(4);
   } else if (cfg->flags & MOE_FWD_SEPARATE_SWIGLU) {
-    if ((rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st)) != MOE_OK) return rc;
+    if ((rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, G, 2 * I, MOE_DTYPE_BF16, st, 0, 0.f, nullptr, nullptr, 0,
+                           nullptr, nullptr, no_mc)) != MOE_OK)
+      return rc;
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
   } else if (pair_gu) {
     // CTA-pair kernel: the gathered token rows are first copied into expert order (x_sorted), so
     // the GEMM loads contiguous rows with tiled TMA boxes
     rc = gemm_checked(x_sorted, R, H, nullptr, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit,
-                      ready, nullptr, 0, nullptr, &producer_tiles);
+                      ready, nullptr, 0, nullptr, &producer_tiles, no_mc);
     if (rc != MOE_OK) return rc;
     ev(4);
   } else {
     // the gate/up launch reports how many of its CTA tiles cover one activation row (single-CTA
     // kernel: one per 128 activation columns; CTA pairs: two per 128)
     rc = gemm_checked(xg, T, H, sti, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit, ready,
-                      nullptr, 0, nullptr, &producer_tiles);
+                      nullptr, 0, nullptr, &producer_tiles, no_mc);
     if (rc != MOE_OK) return rc;
     ev(4);
   }
   ev(5);
   rc = small ? gemv_checked(act, R, I, nullptr, w_down, off, R, Y, H, 0, 0.f, st)
              : gemm_checked(act, R, I, nullptr, w_down, off, R, Y, H, MOE_DTYPE_BF16, st, 0, 0.f, nullptr, ready,
-                            producer_tiles, ready ? ready + E : nullptr);
+                            producer_tiles, ready ? ready + E : nullptr, nullptr, no_mc);
   if (rc != MOE_OK) return rc;
   ev(6);
   if (shared_ready && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(shared_ready), 0) != cudaSuccess)

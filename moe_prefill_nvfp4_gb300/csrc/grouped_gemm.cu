@@ -698,12 +698,13 @@ int launch_cfg(const CUtensorMap& amap, const GemmArgs& args, cudaStream_t strea
   // groups, not only powers of two) makes each tile cheaper.  Wide clusters leave SMs idle (8-CTA
   // clusters fit on 120 of 152 SMs, 6-CTA on 138), which measured as the lesser cost down to ~90%
   // coverage: gathered rows take the widest width whose clusters cover >= 90% of the SMs.
-  // Contiguous rows in tiled boxes use pairs.
+  // Contiguous rows in tiled boxes use pairs.  args.max_cluster caps the width (1: every CTA
+  // loads its own activation tiles, no multicast).
   const int nblocks = (args.N + BM - 1) / BM;
   const int groups = nblocks / C::NBLK;
   const bool gathered = args.gather != nullptr;
   int CL = 1, ncl_max = 0;
-  for (int cl = gathered ? 8 : 2; cl >= 1; --cl) {
+  for (int cl = std::min(gathered ? 8 : 2, std::max(1, args.max_cluster)); cl >= 1; --cl) {
     if (groups % cl != 0) continue;
     int n = max_clusters[dev][cl].load(std::memory_order_relaxed);
     if (n == 0) {

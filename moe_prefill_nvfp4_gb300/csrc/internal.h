@@ -40,6 +40,8 @@ struct GemmArgs {
   const int* ready_in;
   int ready_need;
   int* tile_counter;
+  // widest thread-block cluster the single-CTA kernel may take (1: no multicast activation loads)
+  int max_cluster;
 };
 
 // Host: encode a tiled tensor map through the driver entry point (no libcuda link needed).

@@ -739,7 +739,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_DESC))
-    ap.add_argument("--reports", default="c1,c2,c0,c4",
+    ap.add_argument("--reports", default="c1,c2,c1s,c0,c4",
                     help="extra workloads in the same line: any of c0,c1,c2,c1s,c4 (comma-separated) or none")
     ap.add_argument("--sweep-rows", default=None, help="row counts of the c4 sweep (default: all eleven)")
     ap.add_argument("--sweep-only", action="store_true",

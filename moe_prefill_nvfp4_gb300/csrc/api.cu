@@ -591,8 +591,10 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   if (rc != MOE_OK) return rc;
   if (current_device() != w_gate_up->device || current_device() != w_down->device) return MOE_ERR_INVALID_ARG;
   // x and logits_in may be host memory the device can read, out host memory it can write: the
-  // router kernel stages a host x into the workspace as it reads it (without a router, one
-  // copy does), the top-k reads host logits directly, the combine stores into host memory
+  // router kernel stages a host x into the workspace as it reads it (without a router, a staging
+  // kernel does, or, when the CTA-pair gate/up GEMM takes the rows in expert order, the kernel
+  // that stores each token row to its sorted positions reads it from the host once), the top-k
+  // reads host logits directly, the combine stores into host memory
   const MemKind x_kind = memory_kind(x);
   if (x_kind == kMemNone || memory_kind(out) == kMemNone) return MOE_ERR_INVALID_ARG;
   if (logits_in && memory_kind(logits_in) == kMemNone) return MOE_ERR_INVALID_ARG;
@@ -624,9 +626,6 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   };
 
   ev(0);
-  if (x_stage && !w_router &&
-      cudaMemcpyAsync(x_stage, x, (size_t)T * H * 2, cudaMemcpyDefault, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
   if (w_router && E <= kRouterTopkMaxE) {
     // router GEMM and top-k in one launch (stage 1 -> 2 is empty): same results as the two
     // standalone entry points
@@ -661,7 +660,13 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
                        (gemm_mode == MOE_GEMM_KERNEL_PAIR ||
                         (gemm_mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, E)));
   uint16_t* x_sorted = reinterpret_cast<uint16_t*>(base + L.x_sorted);
-  if (pair_gu && (rc = gather_rows_launch(xg, T, H, sti, off, E, R, H, x_sorted, err, st)) != MOE_OK) return rc;
+  if (pair_gu && x_stage && !w_router) {
+    // host x, rows in expert order: each row read over the link once, stored k times
+    if ((rc = scatter_rows_launch(x, T, H, t2p, k, R, x_sorted, st)) != MOE_OK) return rc;
+  } else {
+    if (x_stage && !w_router && (rc = stage_rows_launch(x, T, H, x_stage, st)) != MOE_OK) return rc;
+    if (pair_gu && (rc = gather_rows_launch(xg, T, H, sti, off, E, R, H, x_sorted, err, st)) != MOE_OK) return rc;
+  }
   ev(3);
   // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
   if (small) {

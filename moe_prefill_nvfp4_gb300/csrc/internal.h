@@ -65,6 +65,12 @@ int pair_gemm_epilogue_groups(const GemmArgs& args);
 // expert_offsets[E]
 int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
                        const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st);
+// x in host memory, read by the device's own loads: stage_rows copies x [T, H] into dst;
+// scatter_rows stores each token row to its k sorted positions xs[token_to_perm[t, s]] (rows of
+// unused slots, position -1, are not written); k <= 32
+int stage_rows_launch(const uint16_t* x, int T, int H, uint16_t* dst, cudaStream_t st);
+int scatter_rows_launch(const uint16_t* x, int T, int H, const int32_t* token_to_perm, int k, int R, uint16_t* xs,
+                        cudaStream_t st);
 int pair_gemm_launch(const GemmArgs& args, cudaStream_t stream);
 // Bound of the pipeline waits of the GEMM kernels (2 s; a debug entry point may lower it).
 uint64_t gemm_wait_limit_ns();

@@ -251,14 +251,16 @@ def test_forward_graph_capture_replay():
     db.close()
 
 
-@pytest.mark.parametrize("routing,E", [("biased", 12), ("router", 12), ("router", 80)],
-                         ids=["host-logits", "router-fused-topk", "router-e80"])
-def test_host_memory_inputs_and_output(routing, E):
+@pytest.mark.parametrize("routing,T,E,k", [("biased", 96, 12, 4), ("router", 96, 12, 4), ("router", 96, 80, 4),
+                                            ("biased", 600, 4, 2)],
+                         ids=["host-logits", "router-fused-topk", "router-e80", "host-logits-rows-in-expert-order"])
+def test_host_memory_inputs_and_output(routing, T, E, k):
     """x, logits and out may be page-locked host memory: a host x is staged into the workspace
-    (by the router kernel, or by one copy without a router), host logits are read in place, the
-    combine stores into the host out.  Eagerly and inside a captured graph the result equals the
-    device-memory run bit for bit."""
-    c = S.make_block_case(T=96, H=512, I=256, E=E, k=4, routing=routing, seed=36)
+    (by the router kernel, or without a router by a staging kernel; with ~300 rows per expert the
+    CTA-pair gate/up GEMM takes its rows in expert order, and the kernel storing them reads each
+    host row once), host logits are read in place, the combine stores into the host out.  Eagerly
+    and inside a captured graph the result equals the device-memory run bit for bit."""
+    c = S.make_block_case(T=T, H=512, I=256, E=E, k=k, routing=routing, seed=36)
     db = DeviceBlock(c)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -277,8 +279,15 @@ def test_host_memory_inputs_and_output(routing, E):
     run()
     s.synchronize()
     assert torch.equal(host.view(torch.int16), ref.view(torch.int16))
-    staged = db.ws_view("x_stage", torch.bfloat16, (c.T, c.H))
-    assert torch.equal(staged.cpu().view(torch.int16), x_host.view(torch.int16))
+    R = c.T * c.k
+    if R / c.E > 128:  # the rows in expert order, each host row stored to its sorted positions
+        sti = db.ws_view("sorted_token_ids", torch.int32, (R,)).cpu().long()
+        n = int(db.ws_view("expert_offsets", torch.int32, (c.E + 1,))[c.E].item())
+        rows = db.ws_view("x_sorted", torch.bfloat16, (R, c.H))[:n].cpu()
+        assert torch.equal(rows.view(torch.int16), x_host[sti[:n]].view(torch.int16))
+    else:
+        staged = db.ws_view("x_stage", torch.bfloat16, (c.T, c.H))
+        assert torch.equal(staged.cpu().view(torch.int16), x_host.view(torch.int16))
     host.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):

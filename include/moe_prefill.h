@@ -186,6 +186,10 @@ int moe_sort_by_expert_noalloc(const int32_t* ids, int T, int k, int E, int32_t*
  *   C            device [R, ldc] of c_dtype (output), ldc >= N
  * Requirements: lda % 8 == 0, ldc % 8 == 0, A and C 16-byte aligned, R >= 1.
  * The kernel reads expert_offsets on the device: no host round trip, graph-capturable.
+ * Kernels: up to ~128 rows per expert (or with gather_ids) single-CTA tiles whose thread-block
+ * clusters share activation tiles through cluster-multicast TMA loads; above that, and for
+ * contiguous rows with N % 256 == 0 and K % 256 == 0, CTA pairs (tcgen05 cta_group::2).  A run on
+ * more than one GPU uses moe_prefill_forward with MOE_FWD_NO_MULTICAST instead.
  */
 int moe_w4a16_grouped_gemm(const uint16_t* A, int a_rows, int lda, const int32_t* gather_ids,
                            const moe_expert_table* W, const int32_t* expert_offsets, int R, void* C, int ldc,
@@ -326,7 +330,10 @@ size_t moe_workspace_bytes(const moe_prefill_config* cfg, int max_rows);
  *   x          BF16 [T, H], device memory or host memory the device can read (page-locked, or
  *              any host memory where the device has pageable memory access): a host x is staged
  *              into the workspace's x_stage by the router kernel as it reads it (without a router,
- *              by one copy on `stream`), and the expert GEMMs read the staged rows
+ *              by a staging kernel), and the expert GEMMs read the staged rows; when the CTA-pair
+ *              gate/up GEMM takes its rows in expert order (more than 128 rows per expert) and
+ *              there is no router, the kernel that stores those rows reads each host row once
+ *              and x_stage stays unused
  *   w_router   device BF16 [E, H] or NULL
  *   logits_in  FP32 [T, E] or NULL (exactly one of w_router / logits_in); device memory or host
  *              memory the device can read (the top-k reads it in place)
@@ -369,7 +376,7 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
  * `ready`: INT32 [E + 1], per-expert counters through which the down GEMM starts on an expert as
  * soon as the gate/up GEMM has stored its activation rows, and the down GEMM's dynamic tile
  * counter (cleared by the sort on every call).  `x_stage`: BF16 [T, H], the device copy of an x
- * passed in host memory (unused when x is device memory).  `x_sorted`: BF16 [T * top_k, H], the
+ * passed in host memory (unused when x is device memory, and on the host-x CTA-pair path above).  `x_sorted`: BF16 [T * top_k, H], the
  * token rows in expert order (row p = x[sorted_token_ids[p]]) that the CTA-pair gate/up GEMM
  * reads (unused with the single-CTA kernel, which gathers inside the GEMM). */
 typedef struct {

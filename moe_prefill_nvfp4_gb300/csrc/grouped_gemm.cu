@@ -68,11 +68,14 @@ constexpr int NTR = 8;           // tile-ring slots of the dynamic scheduler
 
 // BN_MAX: token-tile width (MMA N, at most 256); NA/NW: activation/weight ring depths;
 // ND: accumulator buffers per block (2 lets the epilogue of one tile overlap the next tile's
-// MMAs); NBLK: 128-row weight blocks per CTA; NDQ: dequantising warpgroups (1 or 2).  TMEM:
+// MMAs); NBLK: 128-row weight blocks per CTA; NDQ: dequantising warpgroups (1 or 2); WU: the MMA
+// warps walk their schedule warp-uniformly and one elected lane issues (else lane 0 alone runs
+// the loop; measured per config: faster with the 48-row tiles, slower with the 128-row ones).  TMEM:
 // ND*NBLK*BN_MAX accumulator columns, the rest holds NT A stages of 32*NBLK columns (64 k of
 // every block).
-template <int BN_MAX_, int NA_, int NW_, int ND_, int NBLK_, int NDQ_ = 2>
+template <int BN_MAX_, int NA_, int NW_, int ND_, int NBLK_, int NDQ_ = 2, bool WU_ = false>
 struct Cfg {
+  static constexpr bool WU = WU_;
   static constexpr int BN_MAX = BN_MAX_;
   static constexpr int NA = NA_;
   static constexpr int NW = NW_;
@@ -606,7 +609,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ MMA issuers
     const int b = warp - WARP_MMA;  // weight block of this issuer (b < 0: a warp without a role)
-    if (lane == 0 && b >= 0 && b < C::NBLK) {
+    if constexpr (C::WU) {
+      if (b >= 0 && b < C::NBLK) {
+        int ai = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+          int g = 0;
+          if (lane == 0) g = tile_at(it);
+          g = __shfl_sync(0xffffffffu, g, 0);
+          if (g == -2) ok = false;
+          if (g < 0) break;
+          const TileInfo ti = decode_tile<C::BN_MAX, C::NBLK>(g, s_tbase, s_offs, E, CL, rank);
+          const int db = it % C::ND;
+          if (!warp_wait(d_empty(db), ((it / C::ND) & 1) ^ 1, s_abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t idesc = make_idesc_bf16(BM, ti.bn);
+          const uint64_t bdesc0 = make_sdesc_sw128(sbase + C::OFF_ACT);
+          const uint32_t a_tmem0 = tmem_base + C::A_COL + b * 32;
+          const uint32_t d_tmem = tmem_base + D_COL + (db * C::NBLK + b) * C::BN_MAX;
+          for (int kb = 0; kb < KA; ++kb, ++ai) {
+            const int s = ai % C::NA;
+            const int ts = ai % NT;
+            if (!warp_wait(a_full(s), (ai / C::NA) & 1, s_abort, args.err)) { ok = false; break; }
+            if (!C::MERGED && !warp_wait(t_full(ts), (ai / NT) & 1, s_abort, args.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t bdesc = bdesc0 + (uint64_t)((s * C::ACT_STAGE) >> 4);
+            if (elect_one()) {
+              mma4_bf16_ts(d_tmem, a_tmem0 + ts * 32 * C::NBLK, bdesc, idesc, kb != 0);
+              if (CL > 1) mma_commit_mc(a_empty(s), mask);
+              else mma_commit(a_empty(s));
+              if (!C::MERGED) mma_commit(t_empty(ts));
+            }
+            __syncwarp();
+          }
+          if (ok) {
+            if (elect_one()) mma_commit(d_full(db));
+            __syncwarp();
+          }
+        }
+        if (!ok) {
+          if (elect_one()) {
+            mma_commit(drain_bar(b));
+            mbar_wait_drain(drain_bar(b), 0);
+          }
+          __syncwarp();
+        }
+      }
+    } else if (lane == 0 && b >= 0 && b < C::NBLK) {
       int ai = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -658,7 +707,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // token tiles of 48 / 64 / 128 / 256 rows; the 48- to 128-row configs pair two weight blocks per CTA
-using CfgT2 = Cfg<48, 5, 4, 2, 2>;   // NT = 5; two accumulator buffers (mean rows per expert <= 32)
+using CfgT2 = Cfg<48, 5, 4, 2, 2, 2, true>;  // NT = 5; two accumulator buffers (mean rows per expert <= 32)
 using CfgS2 = Cfg<64, 6, 4, 1, 2>;   // NT = 6
 using CfgS2D = Cfg<64, 4, 4, 2, 2>;  // NT = 4; two accumulator buffers (contiguous rows)
 using CfgM2 = Cfg<128, 4, 3, 1, 2, 1>;  // NT = 4; one dequantising warpgroup

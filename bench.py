@@ -394,9 +394,8 @@ class GpuBench:
         dom = "gate_up" if mean_stage[3] >= mean_stage[5] else "down"
         R = T * k
         # the gate/up token rows are copied into expert order first when the CTA-pair GEMM takes them
-        pair_rows = R / E > 128 and (2 * I) % 256 == 0 and H % 256 == 0
         launches = (((2 if E > 64 else 1) if wr is not None else 1) + (1 if R <= 2048 else 2) + 3
-                    + (1 if pair_rows else 0) + (3 if sh is not None else 0))
+                    + (3 if sh is not None else 0))
         res = {
             "workload": WORKLOAD_DESC.get(name, name), "rows": T, "hidden": H, "moe_intermediate": I, "experts": E,
             "top_k": k, "experts_touched": int((np.diff(off[:E + 1]) > 0).sum()),
@@ -412,9 +411,9 @@ class GpuBench:
             "gemm_roofline": gemms,
             "stage_ms": {n: round(float(v), 5) for n, v in zip(names, mean_stage)},
             # routing (router GEMM + top-k as one launch for E <= 64, else two; top-k alone on given
-            # logits), sort (one launch up to 2048 slots, else two), the row copy into expert order
-            # (CTA-pair gate/up GEMM only), gate/up GEMM with the fused SwiGLU, down GEMM, combine
-            # (+ the shared expert's gate/up GEMM, SwiGLU and down GEMM)
+            # logits), sort (one launch up to 2048 slots, else two), gate/up GEMM with the fused
+            # SwiGLU (the CTA-pair kernel also stores its token rows in expert order), down GEMM,
+            # combine (+ the shared expert's gate/up GEMM, SwiGLU and down GEMM)
             "gpu_launches_per_step": launches,
             "wall_s_timed": round(t_wall, 4),
         }

@@ -373,12 +373,15 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
                         const uint16_t* shared_out, void* shared_ready, void* const* stage_events, void* stream);
 
 /* Byte offsets of the workspace buffers moe_prefill_forward fills (for tests/inspection).
- * `ready`: INT32 [E + 1], per-expert counters through which the down GEMM starts on an expert as
- * soon as the gate/up GEMM has stored its activation rows, and the down GEMM's dynamic tile
- * counter (cleared by the sort on every call).  `x_stage`: BF16 [T, H], the device copy of an x
- * passed in host memory (unused when x is device memory, and on the host-x CTA-pair path above).  `x_sorted`: BF16 [T * top_k, H], the
- * token rows in expert order (row p = x[sorted_token_ids[p]]) that the CTA-pair gate/up GEMM
- * reads (unused with the single-CTA kernel, which gathers inside the GEMM). */
+ * `ready`: INT32 [2E + 1]: [0, E) per-expert counters through which the down GEMM starts on an
+ * expert as soon as the gate/up GEMM has stored its activation rows, [E] the down GEMM's dynamic
+ * tile counter, [E + 1, 2E + 1) the per-expert counts of token rows the CTA-pair gate/up GEMM
+ * has stored in expert order (all cleared by the sort on every call).  `x_stage`: BF16 [T, H],
+ * the device copy of an x passed in host memory (unused when x is device memory, and on the
+ * host-x CTA-pair path above).  `x_sorted`: BF16 [T * top_k, H], the token rows in expert order
+ * (row p = x[sorted_token_ids[p]], for the rows of experts present in w_gate_up) that the CTA-pair
+ * gate/up GEMM stores and reads (unused with the single-CTA kernel, which gathers inside the
+ * GEMM). */
 typedef struct {
   size_t logits, ids, wts, sorted_token_ids, sorted_expert_ids, expert_offsets, token_to_perm, sort_scratch, ready,
       G, act, Y, x_stage, x_sorted, total;
@@ -394,8 +397,8 @@ int moe_workspace_layout(const moe_prefill_config* cfg, int max_rows, moe_worksp
  * moe_debug_set_gemm_kernel: which grouped GEMM kernel the GEMM entry points and the forward
  * launch.  MOE_GEMM_KERNEL_AUTO (the default) takes the CTA-pair kernel where it is faster
  * (experts averaging more than 128 sorted rows) and its shapes allow it (N % 256 == 0; with the
- * fused SwiGLU I % 128 == 0; A rows contiguous -- the forward copies the gate/up GEMM's gathered
- * rows into expert order for it), and the single-CTA kernel otherwise; SINGLE always takes the
+ * fused SwiGLU I % 128 == 0; A rows contiguous -- in the forward the pair kernel stores the gate/up
+ * GEMM's gathered rows in expert order itself), and the single-CTA kernel otherwise; SINGLE always takes the
  * single-CTA kernel; PAIR takes the pair kernel for every shape it allows and makes the entry
  * points return MOE_ERR_UNSUPPORTED_SHAPE for the others.  Returns MOE_ERR_INVALID_ARG for
  * another value.

@@ -354,7 +354,9 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
                         const int32_t* expert_offsets, int R, void* C, int ldc, int c_dtype, cudaStream_t st,
                         int swiglu_half = 0, float limit = 0.f, int* ready_out = nullptr,
                         const int* ready_in = nullptr, int ready_need = 0, int* tile_counter = nullptr,
-                        int* tiles_per_row = nullptr, bool no_multicast = false) {
+                        int* tiles_per_row = nullptr, bool no_multicast = false,
+                        const uint16_t* row_src = nullptr, int row_src_rows = 0, const int32_t* row_ids = nullptr,
+                        int* rows_ready = nullptr) {
   if (A == nullptr || W == nullptr || expert_offsets == nullptr || C == nullptr) return MOE_ERR_INVALID_ARG;
   if (c_dtype != MOE_DTYPE_BF16 && c_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (swiglu_half && (c_dtype != MOE_DTYPE_BF16 || W->N != 2 * swiglu_half || swiglu_half % 128 != 0))
@@ -392,10 +394,18 @@ static int gemm_checked(const uint16_t* A, int a_rows, int lda, const int32_t* g
   a.lda = lda;
   a.wait_ns = gemm_wait_limit_ns();
   a.max_cluster = no_multicast ? 1 : 8;
+  a.row_src = row_src;
+  a.row_src_rows = row_src_rows;
+  a.row_src_ld = lda;
+  a.row_ids = row_ids;
+  a.rows_ready = rows_ready;
   const int mode = g_gemm_kernel.load(std::memory_order_relaxed);
   const bool pair = pair_gemm_supported(a) &&
                     (mode == MOE_GEMM_KERNEL_PAIR || (mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, W->E)));
   if (mode == MOE_GEMM_KERNEL_PAIR && !pair) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // only the pair kernel stores its rows in expert order itself
+  if (row_src != nullptr && (!pair || row_ids == nullptr || rows_ready == nullptr || !aligned16(row_src)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   // CTA tiles of this launch covering one output row (counted once per epilogue warpgroup): the
   // producer side of the forward's GEMM overlap publishes per tile and warp (and, for absent
   // experts' zero rows, this many per row and warp)
@@ -554,7 +564,7 @@ int moe_workspace_layout(const moe_prefill_config* c, int max_rows, moe_workspac
   L->expert_offsets = take((E + 1) * 4);
   L->token_to_perm = take(R * 4);
   L->sort_scratch = take(sort_scratch_bytes((int)R, (int)E));
-  L->ready = take((E + 1) * 4);
+  L->ready = take((2 * E + 1) * 4);
   L->G = take((c->flags & MOE_FWD_SEPARATE_SWIGLU) ? R * 2 * I * 2 : 0);
   L->act = take(R * I * 2);
   L->Y = take(R * H * 2);
@@ -647,25 +657,28 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
   // The fused-SwiGLU tensor-core path runs the down GEMM alongside the gate/up GEMM's last tiles:
   // the down GEMM loads an expert's activation rows once every gate/up CTA tile of them is stored
   // (per-expert counters ready[0..E)), and its clusters take tiles dynamically (counter ready[E]),
-  // so the SMs the gate/up launch leaves early take more of the down work.  The sort clears them.
+  // so the SMs the gate/up launch leaves early take more of the down work.  The CTA-pair gate/up
+  // GEMM stores its token rows in expert order itself and counts them per expert in
+  // ready[E+1..2E+1).  The sort clears all of them.
   const bool small = T <= 8 && (cfg->flags & MOE_FWD_SMALL_ROWS) && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   const bool overlap = !small && !(cfg->flags & MOE_FWD_SEPARATE_SWIGLU);
   const bool no_mc = (cfg->flags & MOE_FWD_NO_MULTICAST) != 0;
   int32_t* ready = overlap ? reinterpret_cast<int32_t*>(base + L.ready) : nullptr;
   int producer_tiles = 0;
-  if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, E + 1)) != MOE_OK) return rc;
+  if ((rc = sort_launch(ids, R, k, E, cnt, sti, sei, off, t2p, err, st, ready, 2 * E + 1)) != MOE_OK) return rc;
   // the fused gate/up GEMM on CTA pairs reads its token rows in expert order
   const int gemm_mode = g_gemm_kernel.load(std::memory_order_relaxed);
   const bool pair_gu = overlap && pair_gemm_shape_ok(2 * I, H, E, I) &&
                        (gemm_mode == MOE_GEMM_KERNEL_PAIR ||
                         (gemm_mode == MOE_GEMM_KERNEL_AUTO && pair_gemm_preferred(R, E)));
   uint16_t* x_sorted = reinterpret_cast<uint16_t*>(base + L.x_sorted);
-  if (pair_gu && x_stage && !w_router) {
-    // host x, rows in expert order: each row read over the link once, stored k times
+  // the pair GEMM stores the rows in expert order from device rows (x, or x_stage written by the
+  // router); a host x without a router is read over the link once instead, each row stored k times
+  const bool host_scatter = pair_gu && x_stage && !w_router;
+  if (host_scatter) {
     if ((rc = scatter_rows_launch(x, T, H, t2p, k, R, x_sorted, st)) != MOE_OK) return rc;
-  } else {
-    if (x_stage && !w_router && (rc = stage_rows_launch(x, T, H, x_stage, st)) != MOE_OK) return rc;
-    if (pair_gu && (rc = gather_rows_launch(xg, T, H, sti, off, E, R, H, x_sorted, err, st)) != MOE_OK) return rc;
+  } else if (x_stage && !w_router && (rc = stage_rows_launch(x, T, H, x_stage, st)) != MOE_OK) {
+    return rc;
   }
   ev(3);
   // at most 8 rows per expert (top-k ids of a token are distinct): the small-row products
@@ -680,10 +693,11 @@ int moe_prefill_forward(const moe_prefill_config* cfg, const uint16_t* x, int T,
     ev(4);
     if ((rc = swiglu_launch(G, G + I, R, I, 2 * I, act, I, cfg->swiglu_limit, st)) != MOE_OK) return rc;
   } else if (pair_gu) {
-    // CTA-pair kernel: the gathered token rows are first copied into expert order (x_sorted), so
-    // the GEMM loads contiguous rows with tiled TMA boxes
+    // CTA-pair kernel: it loads contiguous rows in expert order (x_sorted) with tiled TMA boxes,
+    // and stores them there itself unless the host rows were scattered above
     rc = gemm_checked(x_sorted, R, H, nullptr, w_gate_up, off, R, act, I, MOE_DTYPE_BF16, st, I, cfg->swiglu_limit,
-                      ready, nullptr, 0, nullptr, &producer_tiles, no_mc);
+                      ready, nullptr, 0, nullptr, &producer_tiles, no_mc, host_scatter ? nullptr : xg, T, sti,
+                      ready + E + 1);
     if (rc != MOE_OK) return rc;
     ev(4);
   } else {

@@ -42,6 +42,16 @@ struct GemmArgs {
   int* tile_counter;
   // widest thread-block cluster the single-CTA kernel may take (1: no multicast activation loads)
   int max_cluster;
+  // Rows in expert order stored by the CTA-pair kernel itself (row_src NULL: A holds them
+  // already).  Its epilogue warps store A[p, :] = row_src[row_ids[p], :] (row stride row_src_ld)
+  // for the sorted rows p of present experts while they have no accumulator to drain, and add 1
+  // to rows_ready[e] (zero at launch) per stored row of expert e; the B producer loads expert e's
+  // rows once rows_ready[e] reaches its row count.  A token id outside [0, row_src_rows) records
+  // MOE_DEVERR_BAD_GATHER and stores token row 0.
+  const uint16_t* row_src;
+  int row_src_rows, row_src_ld;
+  const int32_t* row_ids;
+  int* rows_ready;
 };
 
 // Host: encode a tiled tensor map through the driver entry point (no libcuda link needed).
@@ -61,10 +71,6 @@ bool pair_gemm_preferred(int R, int E);
 // epilogue warpgroups of the pair kernel config the launch takes (each of their warps publishes
 // a tile's rows to the forward's GEMM overlap)
 int pair_gemm_epilogue_groups(const GemmArgs& args);
-// token rows in expert order (the pair GEMM's contiguous A): xs[p] = x[sorted_token_ids[p]], p <
-// expert_offsets[E]
-int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
-                       const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st);
 // x in host memory, read by the device's own loads: stage_rows copies x [T, H] into dst;
 // scatter_rows stores each token row to its k sorted positions xs[token_to_perm[t, s]] (rows of
 // unused slots, position -1, are not written); k <= 32

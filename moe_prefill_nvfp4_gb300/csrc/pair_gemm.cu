@@ -16,14 +16,18 @@
 // it slower, so small MMAs leave the tensor pipe idle.
 //
 // B rows are contiguous: the down GEMM's activation rows are already in expert order, and the
-// forward copies the gate/up GEMM's gathered token rows into expert order first (one copy kernel;
+// gate/up GEMM's gathered token rows are stored into expert order by this kernel's own epilogue
+// warps, which have nothing to drain until the first accumulators are complete (GemmArgs::row_src;
 // a TMA gather4 moves only ~12 B/cycle per SM and a 256-token tile needs ~32 B/cycle, 16-byte
-// cp.async gathers from two warps measured ~8 B/cycle).  Each CTA loads the rows it holds with
-// one tiled TMA box per atom (BN/2 rows x 64 k, 128-byte swizzle) whose transaction bytes complete
-// on the even CTA's barrier (the .cta_group::2 form).  There is no cluster multicast.
+// cp.async gathers from two warps measured ~8 B/cycle, so the tiles do not gather).  The rows are
+// stored in sorted order by all epilogue warps of the grid; an expert's tiles start once its row
+// count is published.  Each CTA loads the rows it holds with one tiled TMA box per atom (BN/2 rows
+// x 64 k, 128-byte swizzle) whose transaction bytes complete on the even CTA's barrier (the
+// .cta_group::2 form).  There is no cluster multicast.
 //
 // Warp roles (16 warps):
-//   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global
+//   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global;
+//         between accumulators, the token rows in expert order (GemmArgs::row_src)
 //   4-7   dequantisation (8-11 a second warpgroup taking alternate atoms when NDQ = 2)
 //   12    weight producer (TMA: packed 2 x [64 rows x 128 B] swizzled + scales 2 x [64 x 16 B])
 //   13    B producer (TMA: this CTA's half of the token tile)
@@ -185,6 +189,17 @@ MOE_DEV bool wait_counter(const int* p, int need, volatile int* abort_flag, int*
     }
     __nanosleep(200);
   }
+}
+
+// Non-blocking probe of a local barrier's phase (acquire at CTA scope when it has completed).
+MOE_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Arrive on the barrier at offset `bar` of the even CTA (local when this is the even CTA).  The
@@ -437,12 +452,66 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       }
     }
+    // Token rows in expert order (row_src set): the epilogue warps of the grid take the sorted
+    // rows round robin (this warp: rows w, w + nw, ...), so the rows are stored roughly in sorted
+    // order, the order in which the pairs reach the experts' tiles.  A warp stores 4 KB of a row
+    // at a time while its next accumulator is not complete (a complete one waits for at most one
+    // such piece), and the rest after its last tile; the stores wait on nothing, so every row is
+    // stored even while B producers wait for them.
+    const int nepw = 4 * C::NEPI;
+    const int row_step = (int)gridDim.x * nepw;
+    const int nrows = (args.row_src != nullptr && !*s_bad) ? s_offs[E] : 0;
+    const int nv = args.K / 8;  // 16-byte vectors of a row (K % 256 == 0: whole warps)
+    int next_row = (int)blockIdx.x * nepw + h * 4 + q, cur_v = 0;
+    // store rows until the barrier's phase `parity` completes (poll) or none is left
+    auto store_rows = [&](uint32_t bar, uint32_t parity, bool poll) {
+      while (next_row < nrows) {
+        int stop = 0;
+        if (lane == 0) stop = (*s_abort != 0 || (poll && mbar_test_wait(bar, parity))) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, stop, 0)) return;
+        const int p = next_row;
+        int lo = 0, hi = E - 1;  // the expert of sorted row p: the last e with offs[e] <= p
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_offs[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        if (args.packed[lo] == nullptr) {  // no tile reads an absent expert's rows
+          next_row += row_step;
+          continue;
+        }
+        int tok = __ldg(args.row_ids + p);
+        if ((unsigned)tok >= (unsigned)args.row_src_rows) {
+          if (lane == 0 && cur_v == 0) set_error(args.err, MOE_DEVERR_BAD_GATHER);
+          tok = 0;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(args.row_src + (size_t)tok * args.row_src_ld) + cur_v;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(const_cast<void*>(args.A)) + (size_t)p * args.lda) +
+                     cur_v;
+        const int n = nv - cur_v;
+        uint4 r[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (32 * j + lane < n) r[j] = __ldg(src + 32 * j + lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (32 * j + lane < n) dst[32 * j + lane] = r[j];
+        cur_v += 256;
+        if (cur_v >= nv) {  // the row is stored: publish it
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) counter_add_release(args.rows_ready + lo, 1);
+          cur_v = 0;
+          next_row += row_step;
+        }
+      }
+    };
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     for (int it = 0;; ++it) {
       const int g = tile_at(it);
       if (g < 0) break;
       const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
       const int db = it % ND;
+      store_rows(d_full(db), (it / ND) & 1, true);
       if (!warp_wait_local(d_full(db), (it / ND) & 1, s_abort, args.err, limit)) break;
       tc_fence_after();
       const uint32_t dcol = (uint32_t)(db * C::BN);
@@ -583,6 +652,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0) counter_add_release(args.ready_out + t.e, t.cnt);
       }
     }
+    store_rows(0, 0, false);
   } else if (warp >= 4 && warp < 4 + 4 * C::NDQ) {
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
@@ -701,6 +771,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // the producer GEMM has stored every row of this expert (all its CTA tiles' epilogue warps)
           if (!wait_counter(args.ready_in + t.e, (s_offs[t.e + 1] - s_offs[t.e]) * args.ready_need * 4, s_abort,
                             args.err, limit)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        if (args.row_src != nullptr) {
+          // every row of this expert is stored in expert order (the grid's epilogue warps)
+          if (!wait_counter(args.rows_ready + t.e, s_offs[t.e + 1] - s_offs[t.e], s_abort, args.err, limit)) {
             ok = false;
             break;
           }

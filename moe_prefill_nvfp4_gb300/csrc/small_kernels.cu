@@ -662,51 +662,6 @@ int combine_launch(const uint16_t* Y, const int32_t* perm, const float* wts, con
 }
 
 // ------------------------------------------------------------------------------------------------
-// token rows in expert order for the gate/up GEMM: xs[p, :] = x[sorted_token_ids[p], :] for the
-// sorted rows p < expert_offsets[E] (read on the device).  A warp copies one row at a time with
-// four 16-byte loads per lane in flight before their stores (the copy is bound by the write
-// stream).  A token id outside [0, a_rows) records MOE_DEVERR_BAD_GATHER and copies row 0.
-
-constexpr int GATHER_THREADS = 256;
-constexpr int GATHER_WARPS = GATHER_THREADS / 32;
-
-__global__ void __launch_bounds__(GATHER_THREADS)
-    gather_rows_kernel(const uint16_t* __restrict__ x, int a_rows, int lda, const int32_t* __restrict__ sti,
-                       const int32_t* __restrict__ offsets, int E, int R, int H, uint16_t* __restrict__ xs, int* err) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int rows = min(max(__ldg(offsets + E), 0), R);
-  const int nvec = H / 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int p = blockIdx.x * GATHER_WARPS + warp; p < rows; p += gridDim.x * GATHER_WARPS) {
-    int tok = __ldg(sti + p);
-    if ((unsigned)tok >= (unsigned)a_rows) {
-      if (lane == 0) set_error(err, MOE_DEVERR_BAD_GATHER);
-      tok = 0;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * lda);
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)p * H);
-    int v = lane;
-    for (; v + 96 < nvec; v += 128) {
-      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), d = __ldg(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = d;
-    }
-    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
-  }
-}
-
-int gather_rows_launch(const uint16_t* x, int a_rows, int lda, const int32_t* sorted_token_ids,
-                       const int32_t* expert_offsets, int E, int R, int H, uint16_t* xs, int* err, cudaStream_t st) {
-  const int nsm = device_sm_count();
-  const int need = (R + GATHER_WARPS - 1) / GATHER_WARPS;
-  const int grid = std::max(1, std::min(need, (nsm > 0 ? nsm : 148) * 8));
-  return launch_pdl(gather_rows_kernel, dim3(grid), dim3(GATHER_THREADS), 0, st, x, a_rows, lda, sorted_token_ids,
-                    expert_offsets, E, R, H, xs, err);
-}
-
 // x in host memory: the device reads it over the CPU-GPU link with its own loads (each thread
 // four 16-byte loads in flight), which for tens of MB measured faster than a copy-engine copy.
 //   stage_rows: x [T, H] -> dst [T, H] (the workspace's x_stage), any T, H % 8 == 0.
@@ -741,14 +696,17 @@ int stage_rows_launch(const uint16_t* x, int T, int H, uint16_t* dst, cudaStream
                     reinterpret_cast<const uint4*>(x), n, reinterpret_cast<uint4*>(dst));
 }
 
-__global__ void __launch_bounds__(GATHER_THREADS)
+constexpr int SCATTER_THREADS = 256;
+constexpr int SCATTER_WARPS = SCATTER_THREADS / 32;
+
+__global__ void __launch_bounds__(SCATTER_THREADS)
     scatter_rows_kernel(const uint16_t* __restrict__ x, int T, int H, const int32_t* __restrict__ t2p, int k, int R,
                         uint16_t* __restrict__ xs) {
   griddep_wait();
   griddep_launch_dependents();
   const int nvec = H / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * GATHER_WARPS + warp; t < T; t += gridDim.x * GATHER_WARPS) {
+  for (int t = blockIdx.x * SCATTER_WARPS + warp; t < T; t += gridDim.x * SCATTER_WARPS) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     int pos[32];  // k <= 32
     for (int s = 0; s < k; ++s) {
@@ -780,9 +738,9 @@ int scatter_rows_launch(const uint16_t* x, int T, int H, const int32_t* token_to
   if (T == 0) return MOE_OK;
   if (k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int nsm = device_sm_count();
-  const int need = (T + GATHER_WARPS - 1) / GATHER_WARPS;
+  const int need = (T + SCATTER_WARPS - 1) / SCATTER_WARPS;
   const int grid = std::max(1, std::min(need, (nsm > 0 ? nsm : 148) * 8));
-  return launch_pdl(scatter_rows_kernel, dim3(grid), dim3(GATHER_THREADS), 0, st, x, T, H, token_to_perm, k, R, xs);
+  return launch_pdl(scatter_rows_kernel, dim3(grid), dim3(SCATTER_THREADS), 0, st, x, T, H, token_to_perm, k, R, xs);
 }
 
 // ------------------------------------------------------------------------------------------------

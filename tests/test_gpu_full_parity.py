@@ -241,7 +241,7 @@ def test_forward_writes_nothing_outside_its_outputs(routing, T, H, I, E, k, pair
     R = T * k
     used = {"logits": T * E * 4 if routing == "router" else 0, "ids": R * 4, "wts": R * 4, "sorted_token_ids": R * 4,
             "sorted_expert_ids": R * 4, "expert_offsets": (E + 1) * 4, "token_to_perm": R * 4,
-            "ready": (E + 1) * 4, "G": 0, "act": R * I * 2, "Y": R * H * 2, "x_stage": 0,
+            "ready": (2 * E + 1) * 4, "G": 0, "act": R * I * 2, "Y": R * H * 2, "x_stage": 0,
             "x_sorted": R * H * 2 if pair else 0}
     names = ["logits", "ids", "wts", "sorted_token_ids", "sorted_expert_ids", "expert_offsets", "token_to_perm",
              "sort_scratch", "ready", "G", "act", "Y", "x_stage", "x_sorted", "total"]

@@ -1,8 +1,8 @@
 """GPU parity of the CTA-pair grouped GEMM (tcgen05 cta_group::2) against the oracle.
 
-The pair kernel is the default wherever N % 256 == 0 and the A rows are contiguous (the forward
-copies the gate/up GEMM's gathered token rows into expert order first; a standalone call with
-gather_ids takes the single-CTA kernel).  These cases force it (``moe_debug_set_gemm_kernel``) on
+The pair kernel is the default wherever N % 256 == 0 and the A rows are contiguous (in the
+forward the gate/up launch stores its gathered token rows in expert order itself; a standalone
+call with gather_ids takes the single-CTA kernel).  These cases force it (``moe_debug_set_gemm_kernel``) on
 A rows in expert order and compare with the oracle's grouped GEMM on the same BF16 operands
 (FP32 output: only the FP32 summation order differs, so 2e-6 of max|ref|), with the exact
 special case bit for bit, and with the single-CTA kernel.  Shapes cover both tile configurations
@@ -174,8 +174,9 @@ def test_pair_refuses_gathered_rows():
                                                (600, 512, 256, 4, 2, "biased")],
                          ids=["ragged-small", "256-row-block", "300-rows-per-expert"])
 def test_forward_on_the_pair_kernel(T, H, I, E, k, routing):
-    """The whole forward with both GEMMs on CTA pairs (the gate/up token rows copied into expert
-    order first): routing and sort bit-exact, every float stage within the stage-wise bounds."""
+    """The whole forward with both GEMMs on CTA pairs (the gate/up launch storing its token rows in
+    expert order as it runs): routing and sort bit-exact, every float stage within the stage-wise
+    bounds."""
     from test_gpu_forward import _check_full
 
     c = S.make_block_case(T=T, H=H, I=I, E=E, k=k, routing=routing, seed=201 + T)
@@ -195,3 +196,37 @@ def test_forward_pair_expert_absent_only_in_gate_up(T, E):
     with moe.gemm_kernel(PAIR):
         _check_full(c)
         assert moe.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("T,E,absent", [(600, 4, None), (600, 4, 1), (2048, 16, 5), (64, 6, 1)],
+                         ids=["wide-tiles", "wide-tiles-absent", "2048-rows-absent", "128-token-tiles-absent"])
+def test_forward_pair_stores_rows_in_expert_order(T, E, absent):
+    """The pair gate/up launch stores its token rows in expert order itself: row p of x_sorted is
+    x[sorted_token_ids[p]] bit for bit for every row of an expert present in the gate/up table;
+    the rows of an absent expert (no tile reads them) and the rows past expert_offsets[E] keep the
+    workspace's previous bytes."""
+    from gpu_helpers import DeviceBlock
+
+    c = S.make_block_case(T=T, H=512, I=256, E=E, k=2, routing="biased", seed=221 + T + E)
+    if absent is not None:
+        c.gate_up.packed[absent] = None
+        c.gate_up.scales[absent] = None
+    db = DeviceBlock(c)
+    db.ws.fill_(0x5A)
+    with moe.gemm_kernel(PAIR):
+        db.forward()
+        torch.cuda.synchronize()
+    R = T * c.k
+    sti = db.ws_view("sorted_token_ids", torch.int32, (R,)).cpu().long()
+    off = db.ws_view("expert_offsets", torch.int32, (E + 1,)).cpu().long()
+    xs = db.ws_view("x_sorted", torch.int16, (R, c.H)).cpu()
+    x = db.x.cpu().view(torch.int16)
+    fill = torch.full((c.H,), 0x5A5A, dtype=torch.int16)
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if e == absent:
+            assert (xs[lo:hi] == fill).all(), f"rows of absent expert {e} written"
+        else:
+            assert torch.equal(xs[lo:hi], x[sti[lo:hi]]), f"rows of expert {e}"
+    assert (xs[int(off[E]):] == fill).all()
+    db.close()

@@ -393,7 +393,6 @@ class GpuBench:
                                          measured_traffic(tag or name, proj))
         dom = "gate_up" if mean_stage[3] >= mean_stage[5] else "down"
         R = T * k
-        # the gate/up token rows are copied into expert order first when the CTA-pair GEMM takes them
         launches = (((2 if E > 64 else 1) if wr is not None else 1) + (1 if R <= 2048 else 2) + 3
                     + (3 if sh is not None else 0))
         res = {
@@ -536,7 +535,8 @@ def run_gemm_only(args):
     """Profiling driver: the two grouped GEMMs alone (gate/up with the fused SwiGLU, then down),
     `args.gemm_only` times, on a small Zipf case at GLM widths (40 experts, 4096 rows, top-8:
     every expert takes 256-token tiles; 0.5 GB of weights), sized for an ncu capture.  The token
-    rows are put into expert order with torch indexing (the forward does it with its own copy)."""
+    rows are put into expert order with torch indexing (in the forward the CTA-pair gate/up launch
+    stores them itself)."""
     import torch
 
     import moe_prefill_nvfp4_gb300 as moe

@@ -10,10 +10,13 @@
 // M = 256: each CTA dequantises its own 128 weight rows into its TENSOR MEMORY (tcgen05.st), each
 // holds half of the token tile (N/2 rows of B) in its shared memory, and one thread of the even CTA
 // issues the pair's MMAs; both CTAs' TMEM receive their 128 rows x N of the FP32 accumulator.  A
-// tile is (expert, 256 weight rows, up to BN token rows); with BN = 256 each MMA instruction does
-// four times the work of a 128 x 128 one, which is what keeps the tensor pipe busy: one thread
-// issues an MMA only every ~70-120 cycles, and the dequantising warps on its sub-partition make
-// it slower, so small MMAs leave the tensor pipe idle.
+// tile is (expert, 256 weight rows, up to BN token rows); a 256 x 192 MMA instruction does three
+// times the work of a 128 x 128 one, which is what keeps the tensor pipe busy: one thread issues
+// an MMA only every ~70-120 cycles, and the dequantising warps on its sub-partition make it
+// slower, so small MMAs leave the tensor pipe idle.  A short tile costs nearly as much as a full
+// one (dequantising its weights sets its pace), so busy experts take tiles of up to 384 rows (two
+// MMAs of N = 192 per k16 step into 384 accumulator columns): an expert with m rows costs
+// ceil(m / 384) weight passes instead of ceil(m / 256).
 //
 // B rows are contiguous: the down GEMM's activation rows are already in expert order, and the
 // gate/up GEMM's gathered token rows are stored into expert order by this kernel's own epilogue
@@ -28,7 +31,7 @@
 // Warp roles (16 warps):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global;
 //         between accumulators, the token rows in expert order (GemmArgs::row_src)
-//   4-7   dequantisation (8-11 a second warpgroup taking alternate atoms when NDQ = 2)
+//   4-7   dequantisation (8-11 a second warpgroup taking alternate turns of atoms when NDQ = 2)
 //   12    weight producer (TMA: packed 2 x [64 rows x 128 B] swizzled + scales 2 x [64 x 16 B])
 //   13    B producer (TMA: this CTA's half of the token tile)
 //   14    MMA issuer (even CTA, one thread); TMEM allocation in both CTAs
@@ -60,23 +63,33 @@ constexpr int TMEM_COLS = 512;
 constexpr int WARP_WP = 12, WARP_BP = 13, WARP_MMA = 14;
 constexpr int MAX_E = 512;
 
-// BN: token-tile width (the pair's MMA N, <= 256, each CTA holds BN/2 rows of B); ND:
-// accumulator buffers (2 lets the epilogue of one tile overlap the next tile's MMAs); NDQ:
-// dequantising warpgroups.  TMEM: ND*BN accumulator columns, then NS A stages of 32 columns.
-template <int BN_, int ND_, int NDQ_, int NEPI_ = 1>
+// BN: token-tile width (each CTA holds BN/2 rows of B); NH: MMAs per k16 step across the tile
+// (each of N = BN/NH <= 256, into its own accumulator columns); ND: accumulator buffers (2 lets
+// the epilogue of one tile overlap the next tile's MMAs); NDQ: dequantising warpgroups.  TMEM:
+// ND*BN accumulator columns, then NS A slots of 32 columns.
+template <int BN_, int ND_, int NDQ_, int NEPI_ = 1, int NH_ = 1>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr int ND = ND_;
   static constexpr int NDQ = NDQ_;
   static constexpr int NEPI = NEPI_;  // epilogue warpgroups (2: alternate 32-column chunks)
+  static constexpr int NH = NH_;
+  static constexpr int HN = BN / NH;      // one MMA's N
+  static constexpr int BOXH = HN / 2;     // B rows of one MMA in each CTA (one TMA box per atom)
   // warps: 0-3 epilogue, 4-7 (and 8-11) dequantisation, 12-14 producers and MMA, 16-19 the second
   // epilogue warpgroup when NEPI = 2
   static constexpr int THREADS = (NEPI == 2 ? 20 : 16) * 32;
   static constexpr int BH = BN / 2;
   static constexpr int A_COL = ND * BN;
-  static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A stages = B stages
+  static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A slots = B slots; atom ai takes slot ai % NS
+  // Dequantising warpgroups take turns of APW consecutive atoms (warpgroup (ai / APW) % NDQ): with
+  // APW = 4 a turn is a whole weight stage (256 k), with APW = 2 each warpgroup takes half of
+  // every stage.  NS a multiple of APW * NDQ gives every A slot a single dequantising writer,
+  // whose successive uses of it are one completed phase apart.
+  static constexpr int APW = NS >= 4 * NDQ ? 4 : 2;
+  static constexpr int WG_PER_STAGE = 4 / APW;  // warpgroups reading each weight stage
   static constexpr int NW = 3;
-  static constexpr int B_STAGE = BH * 128;
+  static constexpr int B_STAGE = BH * 128;  // NH boxes of BOXH rows
   static constexpr int PK_STAGE = BM * 128;
   static constexpr int SC_STAGE = BM * 16;
   static constexpr int EPI_WARP_BYTES = 32 * 32 * 4;
@@ -93,16 +106,16 @@ struct Cfg {
   static constexpr int BYTES = OFF_MISC + 32;
   static constexpr int SMEM_ALLOC = BYTES + 1024;
   static constexpr int FULL_COUNT = 2 * 4 + 1;  // dequantising warps of both CTAs + the B producer
-  static_assert(BN % 32 == 0 && BN <= 256 && NS >= 2, "token tile / TMEM columns");
+  static_assert(BN == NH * HN && HN % 32 == 0 && HN <= 256 && (NH == 1 || NH == 2) && NS >= 2,
+                "token tile / TMEM columns");
+  static_assert((BOXH * 128) % 1024 == 0, "B box of one MMA: whole 1 KB swizzle atoms");
   static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
   static_assert((NDQ == 1 || NDQ == 2) && (NEPI == 1 || NEPI == 2), "warpgroups");
-  // A dequantising warpgroup takes whole weight stages (four atoms) and waits on the four atoms'
-  // slots by phase parity; with NS >= 4 NDQ each slot has one writing warpgroup, whose successive
-  // uses of it are a completed phase apart.  Fewer slots let a warpgroup's parity wait pass on the
-  // phase before the one it needs (the other warpgroup's use still pending), which breaks the
-  // barriers' arrival and transaction counts.
-  static_assert(NS >= 4 * NDQ && NS % (4 * NDQ) == 0, "A stages per dequantising warpgroup");
+  // A slot written by two warpgroups would let one's parity wait pass on the phase before the one
+  // it needs (the other's use still pending), which breaks the barriers' arrival and transaction
+  // counts.
+  static_assert(NS % (APW * NDQ) == 0, "A slots per dequantising warpgroup");
 };
 
 struct Tile {
@@ -357,7 +370,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int s = 0; s < NW; ++s) {
       mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), 4);  // the 4 warps of the warpgroup that takes the stage
+      mbar_init(w_empty(s), 4 * C::WG_PER_STAGE);  // the warps of the warpgroups that read the stage
     }
     for (int d = 0; d < ND; ++d) {
       mbar_init(d_full(d), 1);
@@ -657,14 +670,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
     // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
-    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes whole weight stages (256 k, four atoms)
-    // wi with wi % NDQ == wg: it reads the stage's packed bytes and scales into registers once,
-    // releases the stage, then writes the four atoms' BF16 tiles into their TMEM slots and
-    // publishes them after one wait for all eight stores.
+    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes its turns of APW atoms: with APW = 4 the
+    // weight stages wi with wi % NDQ == wg, with APW = 2 atoms 2wg, 2wg + 1 of every stage.  It
+    // reads its part of the stage's packed bytes and scales into registers once, releases the
+    // stage, then writes its atoms' BF16 tiles into their TMEM slots and publishes them after one
+    // wait for all their stores.
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    constexpr int APW = C::APW;
+    const int a_lo = APW == 4 ? 0 : 2 * wg;  // this warpgroup's first atom of a stage it reads
     int wi = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
@@ -673,22 +689,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
       const float s2 = args.scale2[t.e];
       for (int ks = 0; ks < KW; ++ks, ++wi) {
-        if (wi % C::NDQ != wg) continue;
+        if (APW == 4 && wi % C::NDQ != wg) continue;
         const int ws = wi % NW;
         if (!warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
           ok = false;
           break;
         }
+        // 16-byte chunks 2a, 2a + 1 of the row hold atom a's 64 codes; scale bytes 4a..4a+3
         const uint8_t* pk = smem + C::OFF_PK + ws * C::PK_STAGE + sr * 128;
-        uint4 pkv[8];
+        uint4 pkv[2 * APW];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) pkv[c] = *reinterpret_cast<const uint4*>(pk + ((c ^ (sr & 7)) << 4));
-        const uint4 scv = *reinterpret_cast<const uint4*>(smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16);
+        for (int c = 0; c < 2 * APW; ++c)
+          pkv[c] = *reinterpret_cast<const uint4*>(pk + (((2 * a_lo + c) ^ (sr & 7)) << 4));
+        const uint8_t* sc = smem + C::OFF_SC + ws * C::SC_STAGE + sr * 16 + 4 * a_lo;
+        uint32_t scw[APW];
+        if constexpr (APW == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sc);
+          scw[0] = v.x, scw[1] = v.y, scw[2] = v.z, scw[3] = v.w;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(sc);
+          scw[0] = v.x, scw[1] = v.y;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(w_empty(ws));
-        const uint32_t scw[4] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int j = 0; j < APW; ++j) {
+          const int a = a_lo + j;
           const int ai = wi * 4 + a;
           const int s = ai % NS;
           if (!warp_wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) {
@@ -698,15 +724,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tc_fence_after();
           const uint32_t ta = tmem_base + lane_addr + C::A_COL + s * 32;
           {
-            const uint32_t w4[4] = {pkv[2 * a].x, pkv[2 * a].y, pkv[2 * a].z, pkv[2 * a].w};
+            const uint32_t w4[4] = {pkv[2 * j].x, pkv[2 * j].y, pkv[2 * j].z, pkv[2 * j].w};
             uint32_t out[16];
-            dequant32(w4, scw[a], s2, out);
+            dequant32(w4, scw[j], s2, out);
             tmem_st_32x32b_x16(ta, out);
           }
           {
-            const uint32_t w4[4] = {pkv[2 * a + 1].x, pkv[2 * a + 1].y, pkv[2 * a + 1].z, pkv[2 * a + 1].w};
+            const uint32_t w4[4] = {pkv[2 * j + 1].x, pkv[2 * j + 1].y, pkv[2 * j + 1].z, pkv[2 * j + 1].w};
             uint32_t out[16];
-            dequant32(w4, scw[a] >> 16, s2, out);
+            dequant32(w4, scw[j] >> 16, s2, out);
             tmem_st_32x32b_x16(ta + 16, out);
           }
         }
@@ -715,7 +741,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-          for (int a = 0; a < 4; ++a) arrive_leader(full((wi * 4 + a) % NS), rank);
+          for (int j = 0; j < APW; ++j) arrive_leader(full((wi * 4 + a_lo + j) % NS), rank);
       }
     }
     if (!ok) tmem_wait_st();  // no TMEM store of this warp outlives it
@@ -766,7 +792,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int g = tile_at(it);
         if (g < 0) break;
         const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
-        const int y0 = t.p0 + (int)rank * C::BH;
+        const int nh = (C::NH == 2 && t.cnt > C::HN) ? 2 : 1;  // MMAs per k16 step for this tile
+        const int y0 = t.p0 + (int)rank * C::BOXH;
         if (args.ready_in != nullptr) {
           // the producer GEMM has stored every row of this expert (all its CTA tiles' epilogue warps)
           if (!wait_counter(args.ready_in + t.e, (s_offs[t.e + 1] - s_offs[t.e]) * args.ready_need * 4, s_abort,
@@ -787,8 +814,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int kb = 0; kb < KA; ++kb, ++ai) {
           const int s = ai % NS;
           if (!wait_local(empty(s), ((ai / NS) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(full(s), 2u * (uint32_t)C::B_STAGE);
-          tma_load_2d_pair(sbase + C::OFF_B + s * C::B_STAGE, &bmap, kb * BKA, y0, leader_addr(full(s)));
+          if (rank == 0) mbar_arrive_expect_tx(full(s), 2u * (uint32_t)(nh * C::BOXH * 128));
+          for (int hh = 0; hh < nh; ++hh)
+            tma_load_2d_pair(sbase + C::OFF_B + s * C::B_STAGE + hh * (C::BOXH * 128), &bmap, kb * BKA, y0 + hh * C::HN,
+                             leader_addr(full(s)));
         }
       }
       if (!ok) {
@@ -810,9 +839,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int g = tile_at(it);
         if (g < 0) break;
         const int db = it % ND;
+        // MMAs per k16 step: the second (accumulator columns HN..) only when the tile has rows there
+        const int nh = C::NH == 2 && decode<C::BN>(g, s_tbase, s_offs, E, NG).cnt > C::HN ? 2 : 1;
         if (!warp_wait_cluster(d_empty(db), ((it / ND) & 1) ^ 1, s_abort, args.err, limit)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t idesc = make_idesc_bf16(PAIR_ROWS, C::BN);
+        const uint32_t idesc = make_idesc_bf16(PAIR_ROWS, C::HN);
         const uint64_t bdesc0 = make_sdesc_sw128(sbase + C::OFF_B);
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * C::BN);
         for (int kb = 0; kb < KA; ++kb, ++ai) {
@@ -821,7 +852,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tc_fence_after();
           const uint64_t bdesc = bdesc0 + (uint64_t)((s * C::B_STAGE) >> 4);
           if (elect_one()) {
-            mma4_pair(d_tmem, tmem_base + C::A_COL + s * 32, bdesc, idesc, kb != 0);
+            for (int hh = 0; hh < nh; ++hh)
+              mma4_pair(d_tmem + hh * C::HN, tmem_base + C::A_COL + s * 32,
+                        bdesc + (uint64_t)((hh * C::BOXH * 128) >> 4), idesc, kb != 0);
             commit_pair(empty(s));
           }
           __syncwarp();
@@ -852,7 +885,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (args.ready_in != nullptr) griddep_wait();
 }
 
-using CfgWide = Cfg<256, 1, 2, 2>;   // 256-token tiles, one accumulator
+// 384-token tiles for experts averaging more than 128 rows: two MMAs of N = 192 per k16 step into
+// 384 accumulator columns, four A slots (the two dequantising warpgroups take alternate halves of
+// every weight stage), one accumulator.  An expert's m rows take ceil(m / 384) tiles, each
+// dequantising the expert's weights once; 256-token tiles (ceil(m / 256) passes, eight A slots)
+// measured 7% slower on the 8192-row chunk's gate/up launch and 6% on its down launch.
+using CfgWide = Cfg<384, 1, 2, 2, 2>;
 using CfgPair = Cfg<128, 2, 2>;   // 128-token tiles, two accumulator buffers
 
 template <class C>
@@ -861,7 +899,7 @@ int launch_cfg(const GemmArgs& args, cudaStream_t stream) {
   {  // A rows (contiguous, expert order): boxes of BN/2 rows x 64 k, 128-byte swizzle
     const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.a_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)args.lda * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BKA, (cuuint32_t)C::BH};
+    const cuuint32_t box[2] = {(cuuint32_t)BKA, (cuuint32_t)C::BOXH};
     const cuuint32_t estr[2] = {1, 1};
     const int rc = encode_tmap(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(args.A), dims, strides, box,
                                estr, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -914,10 +952,10 @@ bool pair_gemm_shape_ok(int N, int K, int E, int swiglu_half) {
   return N % pg::PAIR_ROWS == 0 && K % pg::BKW == 0 && E <= pg::MAX_E && (swiglu_half == 0 || swiglu_half * 2 == N);
 }
 
-// Measured on GLM widths: the pair kernel's 256-token tiles beat the single-CTA kernel once experts
-// average more than 128 rows (the 8192-row Zipf chunk: gate/up 1.81 vs 2.33 ms, down 1.14 vs
-// 1.23 ms); at ~100 rows per expert (2048 rows, 160 experts) and below the single-CTA kernel's
-// multicast activation tiles are faster (gate/up 0.74 vs 0.95 ms).
+// Measured on GLM widths: the pair kernel's wide tiles beat the single-CTA kernel once experts
+// average more than 128 rows (the 8192-row Zipf chunk, with 256-token tiles: gate/up 1.81 vs
+// 2.33 ms, down 1.14 vs 1.23 ms); at ~100 rows per expert (2048 rows, 160 experts) and below the
+// single-CTA kernel's multicast activation tiles are faster (gate/up 0.74 vs 0.95 ms).
 bool pair_gemm_preferred(int R, int E) { return (double)R / E > 128.0; }
 
 namespace {

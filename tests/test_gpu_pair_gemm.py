@@ -152,6 +152,32 @@ def test_pair_swiglu_fused(T, E, k, I, big, identity):
     assert ok and e < TOL_BF16, e
 
 
+@pytest.mark.parametrize("counts", [(1, 100, 192, 193, 300, 384, 385, 700, 1000), (17, 191, 383, 769, 1152, 5)],
+                         ids=["halves-and-tiles", "ragged"])
+def test_pair_swiglu_384_token_tiles(counts):
+    """With more than 128 rows per expert the fused gate/up launch takes 384-token tiles: two MMAs
+    of N = 192 per k16 step, the second only for tiles with more than 192 rows, and each
+    dequantising warpgroup taking half of every weight stage.  Experts whose rows fill one half,
+    both halves exactly, several tiles with ragged tails, and an absent expert; every element of
+    act within the fused SwiGLU's bound, the absent expert's rows zero."""
+    E = len(counts) + 1
+    T = sum(counts) + 50
+    I = 256
+    c = S.make_gemm_case(T=T, E=E, k=1, N=2 * I, K=512, seed=181 + len(counts), absent=(E - 1,))
+    ids = np.concatenate([np.full(n, e, dtype=np.int32) for e, n in enumerate(list(counts) + [50])])
+    np.random.default_rng(19).shuffle(ids)
+    c.ids = ids.reshape(T, 1)
+    assert T / E > 128
+    act, srt = _run(c, PAIR, swiglu=True, guard=1)
+    G64 = _oracle(c, srt)
+    got = bf16_host(act)
+    o = srt["expert_offsets"]
+    assert list(np.diff(o)) == list(counts) + [50]
+    assert (got[o[E - 1]:o[E]] == 0).all()
+    e, ok = fused_act_error(got, G64, I, 7.0)
+    assert ok and e < TOL_BF16, e
+
+
 def test_pair_refuses_gathered_rows():
     """With gather_ids the pair kernel is not taken: PAIR mode refuses, AUTO takes the single-CTA
     kernel."""

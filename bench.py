@@ -534,7 +534,7 @@ class GpuBench:
 def run_gemm_only(args):
     """Profiling driver: the two grouped GEMMs alone (gate/up with the fused SwiGLU, then down),
     `args.gemm_only` times, on a small Zipf case at GLM widths (40 experts, 4096 rows, top-8:
-    every expert takes 256-token tiles; 0.5 GB of weights), sized for an ncu capture.  The token
+    every expert takes the wide 384-token tiles; 0.5 GB of weights), sized for an ncu capture.  The token
     rows are put into expert order with torch indexing (in the forward the CTA-pair gate/up launch
     stores them itself)."""
     import torch

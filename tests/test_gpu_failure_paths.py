@@ -44,10 +44,10 @@ def _oracle(c, s):
     return O.grouped_gemm(O.bf16_bits_to_f64(c.x), s["expert_offsets"], wfn, s["sorted_token_ids"])
 
 
-@pytest.mark.parametrize("T,E", [(96, 6), (600, 4)], ids=["128-token-tiles", "256-token-tiles"])
+@pytest.mark.parametrize("T,E", [(96, 6), (600, 4)], ids=["128-token-tiles", "384-token-tiles"])
 def test_wait_runs_out_and_the_kernel_returns(T, E):
-    """Both CTA-pair configurations: dequantised weights in tensor memory (16 rows per expert) and
-    in shared memory (300 rows per expert)."""
+    """Both CTA-pair configurations: 128-token tiles with two accumulator buffers (16 rows per
+    expert) and 384-token tiles with one (300 rows per expert)."""
     c, srt, proj = _case(T, E)
     R = c.T * c.k
     x = bf16_dev(c.x)

@@ -6,7 +6,7 @@ call with gather_ids takes the single-CTA kernel).  These cases force it (``moe_
 A rows in expert order and compare with the oracle's grouped GEMM on the same BF16 operands
 (FP32 output: only the FP32 summation order differs, so 2e-6 of max|ref|), with the exact
 special case bit for bit, and with the single-CTA kernel.  Shapes cover both tile configurations
-(128-token tiles with two accumulator buffers, 256-token tiles with one), ragged experts (1 row,
+(128-token tiles with two accumulator buffers, 384-token tiles with one), ragged experts (1 row,
 32k + 1 rows, experts spanning several token tiles), absent and empty experts, and the fused
 SwiGLU.
 """
@@ -88,8 +88,8 @@ def test_pair_exact_dyadic_bit_exact():
     (40, 16, 8, 256, 512, False),      # ~20 rows per expert: 128-token tiles
     (40, 16, 8, 512, 512, True),       # contiguous rows
     (300, 24, 8, 768, 256, False),     # ~100 rows per expert, K = 256 (one weight stage)
-    (600, 4, 2, 512, 768, False),      # ~300 rows per expert: 256-token tiles, several per expert
-    (600, 4, 2, 256, 512, True),       # 256-token tiles, contiguous
+    (600, 4, 2, 512, 768, False),      # ~300 rows per expert: wide (384-token) tiles, both MMA halves
+    (600, 4, 2, 256, 512, True),       # wide tiles, contiguous
     (1030, 3, 1, 256, 512, False),     # ~343 rows, ragged 16k+6 tails
 ], ids=["128tok-gathered", "128tok-contiguous", "100rows-K256", "256tok-gathered", "256tok-contiguous",
         "256tok-ragged"])
@@ -110,7 +110,7 @@ def test_pair_ragged_single_rows_absent_and_empty():
     ids[3:20] = 3
     ids[20:40] = 4
     ids[40:60] = 5
-    ids[60:] = 0  # 340 rows: two 256-token tiles at most
+    ids[60:] = 0  # 340 rows: one 384-token tile
     g.shuffle(ids)
     c.ids = ids
     C, srt = _run(c, PAIR, guard=1)

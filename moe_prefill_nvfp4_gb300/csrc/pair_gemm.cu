@@ -24,13 +24,14 @@
 // a TMA gather4 moves only ~12 B/cycle per SM and a 256-token tile needs ~32 B/cycle, 16-byte
 // cp.async gathers from two warps measured ~8 B/cycle, so the tiles do not gather).  The rows are
 // stored in sorted order by all epilogue warps of the grid; an expert's tiles start once its row
-// count is published.  Each CTA loads the rows it holds with one tiled TMA box per atom (BN/2 rows
-// x 64 k, 128-byte swizzle) whose transaction bytes complete on the even CTA's barrier (the
-// .cta_group::2 form).  There is no cluster multicast.
+// count is published.  Each CTA loads the rows it holds with one tiled TMA box per atom and MMA
+// (BN/(2 NH) rows x 64 k, 128-byte swizzle) whose transaction bytes complete on the even CTA's
+// barrier (the .cta_group::2 form).  There is no cluster multicast.
 //
-// Warp roles (16 warps):
+// Warp roles (16 warps, 20 with a second epilogue warpgroup):
 //   0-3   epilogue: TMEM -> registers -> BF16/FP32 (or the fused clamped SwiGLU) -> global;
-//         between accumulators, the token rows in expert order (GemmArgs::row_src)
+//         between accumulators, the token rows in expert order (GemmArgs::row_src); 16-19 the
+//         second epilogue warpgroup
 //   4-7   dequantisation (8-11 a second warpgroup taking alternate turns of atoms when NDQ = 2)
 //   12    weight producer (TMA: packed 2 x [64 rows x 128 B] swizzled + scales 2 x [64 x 16 B])
 //   13    B producer (TMA: this CTA's half of the token tile)

@@ -99,7 +99,7 @@ def test_workspace_layout(L):
     offs = [lay.logits, lay.ids, lay.wts, lay.sorted_token_ids, lay.sorted_expert_ids, lay.expert_offsets,
             lay.token_to_perm, lay.sort_scratch, lay.ready, lay.G, lay.act, lay.Y, lay.x_stage, lay.x_sorted]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
-    assert lay.G - lay.ready >= 65 * 4
+    assert lay.G - lay.ready >= (2 * 64 + 1) * 4  # per-expert act and row counters, the tile counter
     assert lay.Y - lay.act >= R * 768 * 2 and lay.x_stage - lay.Y >= R * 2048 * 2
     assert lay.x_sorted - lay.x_stage >= 256 * 2048 * 2 and lay.total - lay.x_sorted >= R * 2048 * 2
     assert _lib.moe_workspace_bytes(cfg, 256) == lay.total

@@ -83,12 +83,11 @@ struct Cfg {
   static constexpr int BH = BN / 2;
   static constexpr int A_COL = ND * BN;
   static constexpr int NS = (TMEM_COLS - A_COL) / 32;  // A slots = B slots; atom ai takes slot ai % NS
-  // Dequantising warpgroups take turns of APW consecutive atoms (warpgroup (ai / APW) % NDQ): with
-  // APW = 4 a turn is a whole weight stage (256 k), with APW = 2 each warpgroup takes half of
-  // every stage.  NS a multiple of APW * NDQ gives every A slot a single dequantising writer,
-  // whose successive uses of it are one completed phase apart.
-  static constexpr int APW = NS >= 4 * NDQ ? 4 : 2;
-  static constexpr int WG_PER_STAGE = 4 / APW;  // warpgroups reading each weight stage
+  // The dequantising warpgroups split every weight stage (four atoms): warpgroup wg takes the APW
+  // atoms wg*APW.. of each stage, so each warpgroup waits on every phase of the weight ring in
+  // order and both release each stage.  With NS a multiple of four every A slot then has a
+  // single dequantising writer, whose successive uses of it are one completed phase apart.
+  static constexpr int APW = 4 / NDQ;
   static constexpr int NW = 3;
   static constexpr int B_STAGE = BH * 128;  // NH boxes of BOXH rows
   static constexpr int PK_STAGE = BM * 128;
@@ -113,10 +112,10 @@ struct Cfg {
   static_assert(OFF_PK % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_SC % 128 == 0, "TMA / swizzle alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory");
   static_assert((NDQ == 1 || NDQ == 2) && (NEPI == 1 || NEPI == 2), "warpgroups");
-  // A slot written by two warpgroups would let one's parity wait pass on the phase before the one
-  // it needs (the other's use still pending), which breaks the barriers' arrival and transaction
-  // counts.
-  static_assert(NS % (APW * NDQ) == 0, "A slots per dequantising warpgroup");
+  // A slot (or a weight stage) that two warpgroups take in alternation would let one's parity
+  // wait pass on the phase before the one it needs (the other's use still pending), which breaks
+  // the barriers' arrival and transaction counts.
+  static_assert(NS % 4 == 0, "A slots per dequantising warpgroup");
 };
 
 struct Tile {
@@ -371,7 +370,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int s = 0; s < NW; ++s) {
       mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), 4 * C::WG_PER_STAGE);  // the warps of the warpgroups that read the stage
+      mbar_init(w_empty(s), 4 * C::NDQ);  // the dequantising warps (every warpgroup reads every stage)
     }
     for (int d = 0; d < ND; ++d) {
       mbar_init(d_full(d), 1);
@@ -671,17 +670,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ------------------------------------------------------------------ dequantisation
     // Warp quadrant q dequantises TMEM lanes 32q..32q+31.  Shared-memory row of lane l: plain
     // GEMM 32q + l; fused SwiGLU (gate rows 0-63, up rows 64-127 of the stage) 16q + l for l < 16,
-    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes its turns of APW atoms: with APW = 4 the
-    // weight stages wi with wi % NDQ == wg, with APW = 2 atoms 2wg, 2wg + 1 of every stage.  It
-    // reads its part of the stage's packed bytes and scales into registers once, releases the
-    // stage, then writes its atoms' BF16 tiles into their TMEM slots and publishes them after one
+    // 64 + 16q + (l - 16) otherwise.  Warpgroup wg takes atoms wg*APW .. wg*APW + APW-1 of every
+    // weight stage: it reads their packed bytes and scales into registers once, releases the
+    // stage, then writes the atoms' BF16 tiles into their TMEM slots and publishes them after one
     // wait for all their stores.
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int sr = half ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     constexpr int APW = C::APW;
-    const int a_lo = APW == 4 ? 0 : 2 * wg;  // this warpgroup's first atom of a stage it reads
+    const int a_lo = wg * APW;  // this warpgroup's first atom of each stage
     int wi = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
@@ -690,7 +688,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const Tile t = decode<C::BN>(g, s_tbase, s_offs, E, NG);
       const float s2 = args.scale2[t.e];
       for (int ks = 0; ks < KW; ++ks, ++wi) {
-        if (APW == 4 && wi % C::NDQ != wg) continue;
         const int ws = wi % NW;
         if (!warp_wait_local(w_full(ws), (wi / NW) & 1, s_abort, args.err, limit)) {
           ok = false;
